@@ -1,0 +1,19 @@
+"""Plain float64 CPU oracle of the weight-quantized fused MoE layer.
+
+TEST INFRASTRUCTURE ONLY. This package is the slow, obviously-correct statement
+of what the GPU library computes. Only the test suite, the smoke check and the
+CPU-baseline leg of the benchmark import it; the library never does, and this
+package imports nothing from the library.
+"""
+from .wna16_oracle import (  # noqa: F401
+    unpack_codes,
+    unpack_zeros,
+    halfbits_to_f64,
+    round_to_halfbits,
+    dequantize_expert,
+    align_capacity,
+    moe_align_block_size,
+    silu,
+    fused_moe_per_token,
+    fused_moe_grouped,
+)

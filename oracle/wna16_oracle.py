@@ -1,0 +1,268 @@
+"""Float64 oracle of the fused W4A16 / W8A16 Mixture-of-Experts layer.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the
+benchmark's CPU-baseline leg, never by the library, and it imports nothing of
+the library. It is deliberately plain: explicit shifts and masks, one float64
+matrix-vector product per (token, slot), no blocking or fusion.
+
+What it follows (the pages give prose, no formulas):
+
+* vLLM PR #12185 "[Kernel] add triton fused moe kernel for gptq/awq": one fused
+  MoE over GPTQ/AWQ int4 weights with per-group scales and zero points; its note
+  1 on ``moe_align_block_size`` (per-expert grouping of (token, slot) pairs,
+  padded to the GEMM block size, graph-safe);
+* vLLM PR #6502 "[Model] Add Support for GPTQ Fused MOE", the bug report on
+  ``BLOCK_SIZE_K`` versus the quantization group size: every K index uses the
+  scale of its own group ``k // G``;
+* vLLM ``fused_moe/oracle/int8.py`` (``int8_w8a16_moe_quant_config`` and the
+  channel-strategy schema): int8 weights, symmetric, one scale per output
+  channel;
+* vLLM PR #14138 "optimize performance of gptq marlin kernel when n is small",
+  benchmark script: ``quantize_weights(weight, uint4, group_size=128, zero
+  points)`` and ``is_zp_float=False`` -> unsigned codes with integer zero points.
+
+Stated readings where the pages are silent (each also listed in the design
+notes): codes are packed LSB first along K in int32 words; scales are stored
+group-major ``[E, K/G, N]``; zero points are the true integer zero, packed LSB
+first along N ``[E, K/G, N/pf]``; without a zeros tensor the zero point is
+``2**(bits-1)``; rows ``[0, I)`` of w13 are the gate projection and ``[I, 2I)``
+the up projection; the activation is ``silu(gate) * up``; the output is the
+top-k weighted sum in slot order, rounded once (round-to-nearest-even) to the
+activation dtype. Pair ids outside ``[0, E)`` are dropped.
+
+Half-precision inputs (fp16 or bf16 activations and scales) are passed as their
+raw 16-bit patterns (``uint16`` arrays) with a dtype tag, so that bf16 needs no
+library support and every conversion to float64 is exact.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# ----------------------------------------------------------------------------
+# number formats
+# ----------------------------------------------------------------------------
+
+
+def halfbits_to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact float64 value of raw fp16 or bf16 bit patterns."""
+    b = np.asarray(bits).astype(np.uint16)
+    if dtype == "f16":
+        return b.view(np.float16).astype(np.float64)
+    if dtype == "bf16":
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+def _round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to bf16 (8 significant bits), nearest-even, once."""
+    x = np.asarray(x, dtype=np.float64)
+    finite = np.isfinite(x)
+    m, e = np.frexp(np.where(finite, x, 0.0))  # x = m * 2**e, 0.5 <= |m| < 1
+    # bf16 keeps 8 significant bits for normals (exponent e-1 >= -126); below
+    # that the spacing is fixed at 2**-133 (subnormals).
+    normal = e - 1 >= -126
+    with np.errstate(over="ignore", invalid="ignore"):
+        r_norm = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+        r_sub = np.ldexp(np.rint(np.ldexp(np.where(normal, 0.0, x), 133)), -133)
+    out = np.where(normal, r_norm, r_sub)
+    out = np.where(finite, out, x)
+    with np.errstate(over="ignore"):
+        f32 = out.astype(np.float32)  # exact (8 significant bits) or +-inf
+    return (f32.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def round_to_halfbits(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float64 to fp16/bf16 (nearest-even, single rounding); raw bits."""
+    if dtype == "f16":
+        # numpy converts float64 -> float16 with one correctly rounded step.
+        return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+    if dtype == "bf16":
+        return _round_to_bf16_bits(x)
+    raise ValueError(dtype)
+
+
+# ----------------------------------------------------------------------------
+# unpack and dequantize
+# ----------------------------------------------------------------------------
+
+
+def unpack_codes(words: np.ndarray, bits: int) -> np.ndarray:
+    """Codes from int32 words packed along the last axis, LSB first.
+
+    code of element ``i`` = ``(word[i // pf] >> (bits * (i % pf))) & (2**bits - 1)``
+    with ``pf = 32 // bits``.
+    """
+    pf = 32 // bits
+    mask = (1 << bits) - 1
+    w = np.asarray(words).astype(np.int64) & 0xFFFFFFFF
+    out = np.empty(w.shape[:-1] + (w.shape[-1] * pf,), dtype=np.int64)
+    for i in range(pf):
+        out[..., i::pf] = (w >> (bits * i)) & mask
+    return out
+
+
+def unpack_zeros(zero_words: np.ndarray, bits: int) -> np.ndarray:
+    """Integer zero points ``[..., K/G, N]`` from words packed along N."""
+    return unpack_codes(zero_words, bits)
+
+
+def dequantize_expert(q: np.ndarray, scales_bits: np.ndarray, zero_words, bits: int,
+                      group_size: int, scale_dtype: str) -> np.ndarray:
+    """Float64 weights ``W[n, k] = (u[n, k] - z[k // G, n]) * s[k // G, n]``.
+
+    ``q`` [N, K/pf] int32, ``scales_bits`` [K/G, N] raw half bits, ``zero_words``
+    [K/G, N/pf] int32 or None (zero point ``2**(bits-1)``). ``group_size`` -1
+    means one group per output channel (G = K).
+    """
+    u = unpack_codes(q, bits)  # [N, K]
+    N, K = u.shape
+    G = K if group_size == -1 else group_size
+    assert K % G == 0
+    s = halfbits_to_f64(scales_bits, scale_dtype)  # [K/G, N]
+    assert s.shape == (K // G, N), (s.shape, K, G, N)
+    if zero_words is None:
+        z = np.full((K // G, N), float(1 << (bits - 1)))
+    else:
+        z = unpack_zeros(zero_words, bits).astype(np.float64)  # [K/G, N]
+        assert z.shape == (K // G, N)
+    g_of_k = np.arange(K) // G
+    return (u.astype(np.float64) - z.T[:, g_of_k]) * s.T[:, g_of_k]
+
+
+# ----------------------------------------------------------------------------
+# moe_align_block_size
+# ----------------------------------------------------------------------------
+
+
+def align_capacity(P: int, E: int, block: int) -> int:
+    """Padded-slot capacity: at most min(P, E) experts are non-empty and each
+    pads fewer than ``block`` slots; rounded up to a whole block."""
+    raw = P + min(P, E) * (block - 1)
+    return int(math.ceil(raw / block)) * block
+
+
+def moe_align_block_size(topk_ids: np.ndarray, E: int, block: int):
+    """Group (token, slot) pairs by expert, padded to the GEMM block size.
+
+    Pair ``p = t * topk + j`` (row-major over ``topk_ids[M, topk]``).
+    Returns ``(sorted_ids [cap], expert_ids [cap/block], num_post_pad, counts [E])``:
+    ``cnt[e] = #{p : id_p = e}`` (ids outside [0, E) are dropped);
+    ``padded[e] = ceil(cnt[e]/block) * block``; ``off[e] = sum_{e'<e} padded[e']``;
+    ``sorted_ids[off[e] + r]`` is the r-th smallest pair with id e for r < cnt[e]
+    and the sentinel ``P`` for the padding; ``expert_ids[b] = e`` for the blocks of
+    expert e; slots at or past ``num_post_pad = sum padded`` hold ``P`` and
+    their blocks ``-1``.
+    """
+    ids = np.asarray(topk_ids).reshape(-1).astype(np.int64)
+    P = ids.size
+    cap = align_capacity(P, E, block)
+    counts = np.zeros(E, dtype=np.int64)
+    for p in range(P):
+        if 0 <= ids[p] < E:
+            counts[ids[p]] += 1
+    padded = [((int(c) + block - 1) // block) * block for c in counts]
+    offsets = [0] * E
+    run = 0
+    for e in range(E):
+        offsets[e] = run
+        run += padded[e]
+    num_post_pad = run
+    sorted_ids = np.full(cap, P, dtype=np.int32)
+    fill = list(offsets)
+    for p in range(P):  # ascending p: stable within each expert
+        e = ids[p]
+        if 0 <= e < E:
+            sorted_ids[fill[e]] = p
+            fill[e] += 1
+    expert_ids = np.full(cap // block, -1, dtype=np.int32)
+    for e in range(E):
+        for b in range(offsets[e] // block, (offsets[e] + padded[e]) // block):
+            expert_ids[b] = e
+    return sorted_ids, expert_ids, int(num_post_pad), counts.astype(np.int32)
+
+
+# ----------------------------------------------------------------------------
+# the layer
+# ----------------------------------------------------------------------------
+
+
+def silu(v: np.ndarray) -> np.ndarray:
+    return v / (1.0 + np.exp(-v))
+
+
+def _expert_matrices(L, e, cache):
+    if e not in cache:
+        w13 = dequantize_expert(L["w13_q"][e], L["w13_s"][e],
+                                None if L["w13_z"] is None else L["w13_z"][e],
+                                L["bits"], L["group_size"], L["scale_dtype"])
+        w2 = dequantize_expert(L["w2_q"][e], L["w2_s"][e],
+                               None if L["w2_z"] is None else L["w2_z"][e],
+                               L["bits"], L["group_size"], L["scale_dtype"])
+        cache[e] = (w13, w2)
+    return cache[e]
+
+
+def fused_moe_per_token(L: dict, tokens=None, round_output=True):
+    """The layer, one (token, slot) at a time, in float64.
+
+    ``L`` holds: ``x`` [M, H] raw half bits, ``act_dtype``, ``w13_q`` [E, 2I, H/pf],
+    ``w13_s`` [E, H/G, 2I] raw bits, ``w13_z`` [E, H/G, 2I/pf] or None, ``w2_q``
+    [E, H, I/pf], ``w2_s`` [E, I/G, H], ``w2_z`` [E, I/G, H/pf] or None,
+    ``scale_dtype``, ``bits``, ``group_size``, ``topk_ids`` [M, k], ``topk_w`` [M, k]
+    float32. For each token t and slot j with expert e = ids[t, j] in [0, E):
+    g = W13[e, :I] x_t, u = W13[e, I:] x_t, a = silu(g) * u, y = W2[e] a;
+    out_t = sum_j w[t, j] y_{t,j} in slot order. Returns float64 [T, H], or the
+    raw half bits of its single rounding when ``round_output``.
+    """
+    x = halfbits_to_f64(L["x"], L["act_dtype"])
+    ids = np.asarray(L["topk_ids"])
+    tw = np.asarray(L["topk_w"], dtype=np.float32).astype(np.float64)
+    M, k = ids.shape
+    E = L["w13_q"].shape[0]
+    I = L["w13_q"].shape[1] // 2
+    H = x.shape[1]
+    tokens = range(M) if tokens is None else tokens
+    cache = {}
+    rows = []
+    for t in tokens:
+        acc = np.zeros(H, dtype=np.float64)
+        for j in range(k):
+            e = int(ids[t, j])
+            if not (0 <= e < E):
+                continue
+            w13, w2 = _expert_matrices(L, e, cache)
+            gu = w13 @ x[t]
+            a = silu(gu[:I]) * gu[I:]
+            acc = acc + tw[t, j] * (w2 @ a)
+        rows.append(acc)
+    out = np.stack(rows) if rows else np.zeros((0, H))
+    return round_to_halfbits(out, L["act_dtype"]) if round_output else out
+
+
+def fused_moe_grouped(L: dict, round_output=True):
+    """Same layer, grouped per expert: dequantize one expert at a time and run
+    one float64 matrix product over all of its routed (token, slot) pairs.
+    Identical mathematics to :func:`fused_moe_per_token`; only the loop order
+    differs (the per-slot terms are still added in slot order)."""
+    x = halfbits_to_f64(L["x"], L["act_dtype"])
+    ids = np.asarray(L["topk_ids"])
+    tw = np.asarray(L["topk_w"], dtype=np.float32).astype(np.float64)
+    M, k = ids.shape
+    E = L["w13_q"].shape[0]
+    I = L["w13_q"].shape[1] // 2
+    H = x.shape[1]
+    y = np.zeros((M, k, H), dtype=np.float64)
+    for e in range(E):
+        tt, jj = np.nonzero(ids == e)
+        if tt.size == 0:
+            continue
+        w13, w2 = _expert_matrices(L, e, {})
+        gu = x[tt] @ w13.T
+        a = silu(gu[:, :I]) * gu[:, I:]
+        y[tt, jj] = (a @ w2.T) * tw[tt, jj][:, None]
+    out = np.zeros((M, H), dtype=np.float64)
+    for j in range(k):
+        out = out + y[:, j]
+    return round_to_halfbits(out, L["act_dtype"]) if round_output else out

@@ -1,0 +1,18 @@
+"""Seeded synthetic inputs for the weight-quantized fused MoE layer.
+
+This package only *makes inputs*: activations, router outputs (top-k ids and
+weights) and quantized expert weights in the library's packed layout. It holds
+none of the layer's arithmetic (no dequantization, no GEMM, no activation, no
+combine), so both the CUDA library and the CPU oracle can consume what it makes
+without sharing any of the method's code.
+"""
+from .workloads import (  # noqa: F401
+    WORKLOADS,
+    Workload,
+    LayerInputs,
+    make_layer_inputs,
+    make_routing,
+    make_hidden,
+    quantize_expert,
+    pack_along_last,
+)
