@@ -1,0 +1,165 @@
+/*
+ * wna16_moe.h - C ABI of a fused Mixture-of-Experts layer with weight-only,
+ * group-quantized experts (int4 "W4A16" GPTQ/AWQ style and int8 "W8A16"), for
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The operation. Pages on which this is based:
+ *   - vLLM PR #12185 "[Kernel] add triton fused moe kernel for gptq/awq": one
+ *     fused MoE launch over gptq/awq int4 expert weights instead of one GEMM per
+ *     expert; note 1 of that PR: a shared-memory, CUDA-graph-safe
+ *     moe_align_block_size that scales to DeepSeek-V3's 256 experts.
+ *   - vLLM PR #6502 "[Model] Add Support for GPTQ Fused MOE": the K tile of the
+ *     GEMM must respect the quantization group (bug report on BLOCK_SIZE_K).
+ *   - vLLM fused_moe/oracle/int8.py: int8 W8A16 experts, symmetric, one scale
+ *     per output channel; weights shaped [experts, ..., N, K].
+ *   - vLLM PR #14138 "optimize performance of gptq marlin kernel when n is
+ *     small": uint4 codes, group_size 128, integer zero points; reducing split
+ *     partial results without a grid barrier.
+ *
+ * For M tokens x[t] (hidden size H), top-k expert ids e = ids[t, j] and weights
+ * w[t, j], each expert holding a gate/up matrix W13[e] (2I x H) and a down
+ * matrix W2[e] (H x I):
+ *     g = W13[e][0:I] x_t,  u = W13[e][I:2I] x_t,  a = silu(g) * u,
+ *     y_{t,j} = W2[e] a,    out_t = sum_j w[t, j] * y_{t,j}   (slot order).
+ * Dequantized weight: W[n, k] = (code[n, k] - zero[k / G, n]) * scale[k / G, n].
+ *
+ * Memory layout of the quantized weights (all row-major, little-endian):
+ *   pf = 32 / bits codes per int32 word.
+ *   q      [E, N, K/pf] int32   code of k in bits [bits*(k%pf), +bits) of word k/pf
+ *   scales [E, K/G, N]  fp16 or bf16 (scale_dtype), group-major
+ *   zeros  [E, K/G, N/pf] int32 zero point of row n in bits [bits*(n%pf), +bits)
+ *                       of word n/pf; NULL = symmetric, zero point 2^(bits-1)
+ *   with (N, K) = (2I, H) for w13 (rows [0,I) gate, [I,2I) up) and (H, I) for w2.
+ *   group_size G: a multiple of 64 that divides K, or -1 for one group per
+ *   output channel (G = K).
+ *
+ * Ownership and threading. Every pointer is a non-owning DEVICE pointer on the
+ * current CUDA device unless stated otherwise, 16-byte aligned. The library
+ * never allocates, frees or synchronizes device memory (except
+ * wna16_read_device_status, which synchronizes the given stream). All compute
+ * calls are asynchronous on `stream` (a cudaStream_t; NULL = default stream),
+ * issue no host synchronization and, with fixed arguments, can be captured in a
+ * CUDA graph and replayed.
+ *
+ * Errors. Argument errors are detected on the host and returned before
+ * anything is launched. Launch failures return WNA16_ERR_CUDA. Errors found on
+ * the device (an expert id outside [0, E), a pipeline wait that gave up) do not
+ * trap: the offending pair is dropped or the kernel returns early, and a bit is
+ * set in the status word at the start of the workspace (read it with
+ * wna16_read_device_status).
+ */
+#ifndef WNA16_MOE_H_
+#define WNA16_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WNA16_OK = 0,
+  WNA16_ERR_INVALID_ARG = 1,          /* null pointer, bad size or alignment */
+  WNA16_ERR_UNSUPPORTED = 2,          /* valid but not supported (shape, bits, G) */
+  WNA16_ERR_WORKSPACE_TOO_SMALL = 3,
+  WNA16_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
+  WNA16_ERR_DEVICE_BAD_EXPERT_ID = 5, /* device: an id outside [0, E) was dropped */
+  WNA16_ERR_DEVICE_TIMEOUT = 6        /* device: a pipeline wait gave up */
+} wna16_status;
+
+typedef enum { WNA16_F16 = 0, WNA16_BF16 = 1 } wna16_dtype;
+
+/* Device status bits (the int32 at offset 0 of the fused-call workspace). */
+#define WNA16_DEV_BAD_EXPERT_ID 0x1
+#define WNA16_DEV_TIMEOUT 0x2
+
+/*
+ * Capacity of the align outputs: an upper bound on padded slots for
+ * num_pairs = M * topk pairs over E experts and GEMM block size `block`:
+ * roundup(num_pairs + min(num_pairs, E) * (block - 1), block).
+ * (Every non-empty expert pads fewer than `block` slots.) Returns -1 on bad
+ * arguments.
+ */
+int64_t wna16_align_capacity(int64_t num_pairs, int E, int block);
+
+/*
+ * moe_align_block_size (vLLM PR #12185, note 1; one CTA, shared-memory
+ * histogram, warp-level ranking, block scan; graph-safe).
+ *   topk_ids   [M, topk] int32 expert id per (token, slot); pair p = t*topk + j.
+ *   sorted_ids [cap] int32 out: pairs grouped by expert in ascending expert
+ *              order, ascending pair index within an expert, each expert padded
+ *              to a multiple of `block` with the sentinel M*topk; slots past the
+ *              padded total hold the sentinel. cap = wna16_align_capacity(...).
+ *   expert_ids [cap / block] int32 out: expert of each block, -1 past the end.
+ *   num_tokens_post_padded [1] int32 out: padded total (a multiple of block).
+ *   expert_counts [E] int32 out, optional (NULL): pairs per expert.
+ *   device_status [1] int32, optional (NULL): reset to 0 by this call, then
+ *              WNA16_DEV_BAD_EXPERT_ID is or-ed in if an id is outside [0, E)
+ *              (that pair is dropped).
+ *   block: a power of two in [16, 256]. E in [1, 256]. M*topk < 2^31.
+ */
+wna16_status wna16_moe_align_block_size(const int32_t* topk_ids, int64_t M, int topk, int E,
+                                        int block, int32_t* sorted_ids, int32_t* expert_ids,
+                                        int32_t* num_tokens_post_padded, int32_t* expert_counts,
+                                        int32_t* device_status, void* stream);
+
+/*
+ * Block size the fused call uses when given block = 0: the power of two in
+ * [16, 256] closest to the expected pairs per active expert.
+ */
+int wna16_choose_block(int64_t M, int topk, int E);
+
+/*
+ * Bytes of workspace wna16_fused_moe needs for these sizes on the current
+ * device (block = 0: the automatic choice, split_k = 0: automatic). Returns 0
+ * on bad arguments.
+ */
+size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, int topk,
+                                       int bits, int group_size, int block, int split_k);
+
+/*
+ * The fused layer: align -> gate/up GEMM with in-kernel dequant and
+ * silu(gate)*up -> down GEMM with in-kernel dequant and the top-k weight ->
+ * ordered top-k combine. One launch per stage (4 launches), none per expert.
+ *   hidden       [M, H] act_dtype.
+ *   w13_q/w13_scales/w13_zeros, w2_q/w2_scales/w2_zeros: layout above
+ *                (zeros may be NULL; both NULL or both non-NULL).
+ *   scale_dtype  dtype of both scale tensors.
+ *   bits         4 or 8. group_size: multiple of 64 dividing H and I, or -1.
+ *   topk_ids     [M, topk] int32; topk_weights [M, topk] fp32.
+ *   out          [M, H] act_dtype, written (never read).
+ *   workspace    device memory of at least wna16_fused_moe_workspace_bytes();
+ *                its first int32 is the device status word (reset by the call).
+ *   block        align block size (0 = automatic), as in
+ *                wna16_moe_align_block_size; it is also the GEMM token tile.
+ *   split_k      K-splits of the down GEMM (0 = automatic, else 1..8).
+ * Shapes: H a multiple of 64, I a multiple of 64, 1 <= topk <= E <= 256,
+ * M*topk < 2^31. M = 0 returns WNA16_OK and launches nothing.
+ */
+wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
+                             int64_t I, int E, int topk, const int32_t* w13_q,
+                             const void* w13_scales, const int32_t* w13_zeros,
+                             const int32_t* w2_q, const void* w2_scales,
+                             const int32_t* w2_zeros, wna16_dtype scale_dtype, int bits,
+                             int group_size, const int32_t* topk_ids,
+                             const float* topk_weights, void* out, void* workspace,
+                             size_t workspace_bytes, int block, int split_k, void* stream);
+
+/*
+ * Synchronizes `stream`, then reads the device status word at the start of a
+ * fused-call workspace (or any int32 status word the caller passed to the
+ * align call). Writes the raw bits to *bits_out (may be NULL) and returns
+ * WNA16_OK, WNA16_ERR_DEVICE_TIMEOUT or WNA16_ERR_DEVICE_BAD_EXPERT_ID
+ * (timeout wins), or WNA16_ERR_CUDA if the copy fails. For tests and debugging.
+ */
+wna16_status wna16_read_device_status(const void* status_word, int32_t* bits_out, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* wna16_status_string(wna16_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WNA16_MOE_H_ */

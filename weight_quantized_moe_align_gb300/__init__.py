@@ -1,0 +1,17 @@
+"""Fused weight-only-quantized (W4A16 / W8A16) Mixture-of-Experts layer for one
+GB300 GPU: a C-ABI CUDA library (``include/wna16_moe.h``) and its binding.
+"""
+from .binding import (  # noqa: F401
+    DEV_BAD_EXPERT_ID,
+    DEV_TIMEOUT,
+    EXPORTED,
+    WNA16Error,
+    align_capacity,
+    choose_block,
+    fused_moe,
+    load,
+    moe_align_block_size,
+    read_device_status,
+    workspace_bytes,
+)
+from .build import LIB, build  # noqa: F401

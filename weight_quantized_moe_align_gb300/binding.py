@@ -1,0 +1,201 @@
+"""Thin ctypes binding of ``include/wna16_moe.h``.
+
+Argument marshalling only: each function checks the torch tensors it is given
+(device, dtype, shape, contiguity), passes their device pointers and the
+current CUDA stream to the C ABI, and raises on a non-OK status. Every step of
+the layer runs in the library's CUDA kernels; there is no other code path. If
+the library has not been built this module raises instead of computing
+anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB
+
+WNA16_OK = 0
+STATUS_NAMES = {
+    0: "WNA16_OK", 1: "WNA16_ERR_INVALID_ARG", 2: "WNA16_ERR_UNSUPPORTED",
+    3: "WNA16_ERR_WORKSPACE_TOO_SMALL", 4: "WNA16_ERR_CUDA",
+    5: "WNA16_ERR_DEVICE_BAD_EXPERT_ID", 6: "WNA16_ERR_DEVICE_TIMEOUT",
+}
+DEV_BAD_EXPERT_ID = 0x1
+DEV_TIMEOUT = 0x2
+
+# Every symbol include/wna16_moe.h declares.
+EXPORTED = (
+    "wna16_align_capacity", "wna16_moe_align_block_size", "wna16_choose_block",
+    "wna16_fused_moe_workspace_bytes", "wna16_fused_moe", "wna16_read_device_status",
+    "wna16_status_string",
+)
+
+_DTYPE = {torch.float16: 0, torch.bfloat16: 1}
+
+
+class WNA16Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Loads the built library (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB):
+        raise RuntimeError(
+            f"CUDA library not built ({LIB}); run `python -m weight_quantized_moe_align_gb300.build`")
+    L = ctypes.CDLL(LIB)
+    c = ctypes
+    vp, i64, i32, sz = c.c_void_p, c.c_int64, c.c_int, c.c_size_t
+    L.wna16_align_capacity.argtypes = [i64, i32, i32]
+    L.wna16_align_capacity.restype = i64
+    L.wna16_choose_block.argtypes = [i64, i32, i32]
+    L.wna16_choose_block.restype = i32
+    L.wna16_moe_align_block_size.argtypes = [vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    L.wna16_moe_align_block_size.restype = i32
+    L.wna16_fused_moe_workspace_bytes.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32]
+    L.wna16_fused_moe_workspace_bytes.restype = sz
+    L.wna16_fused_moe.argtypes = [vp, i32, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, i32, i32,
+                                  i32, vp, vp, vp, vp, sz, i32, i32, vp]
+    L.wna16_fused_moe.restype = i32
+    L.wna16_read_device_status.argtypes = [vp, c.POINTER(c.c_int32), vp]
+    L.wna16_read_device_status.restype = i32
+    L.wna16_status_string.argtypes = [i32]
+    L.wna16_status_string.restype = c.c_char_p
+    _lib = L
+    return L
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype=None, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _raise(st: int, what: str):
+    if st != WNA16_OK:
+        raise WNA16Error(st, what)
+
+
+def align_capacity(num_pairs: int, E: int, block: int) -> int:
+    return int(load().wna16_align_capacity(num_pairs, E, block))
+
+
+def choose_block(M: int, topk: int, E: int) -> int:
+    return int(load().wna16_choose_block(M, topk, E))
+
+
+def workspace_bytes(M, H, I, E, topk, bits, group_size, block=0, split_k=0) -> int:
+    n = int(load().wna16_fused_moe_workspace_bytes(M, H, I, E, topk, bits, group_size, block, split_k))
+    if n == 0 and M > 0:
+        raise WNA16Error(1, "wna16_fused_moe_workspace_bytes")
+    return n
+
+
+def moe_align_block_size(topk_ids: torch.Tensor, E: int, block: int, with_counts=True,
+                         status: Optional[torch.Tensor] = None, out=None, stream=None):
+    """Returns (sorted_ids [cap], expert_ids [cap/block], num_tokens_post_padded [1],
+    expert_counts [E] or None) as int32 CUDA tensors."""
+    _check(topk_ids, "topk_ids", torch.int32)
+    if topk_ids.dim() != 2:
+        raise ValueError("topk_ids must be [M, topk]")
+    M, topk = topk_ids.shape
+    dev = topk_ids.device
+    cap = align_capacity(M * topk, E, block)
+    if cap < 0:
+        raise WNA16Error(1, "wna16_align_capacity")
+    if out is None:
+        sorted_ids = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+        expert_ids = torch.empty(max(cap // block, 1), dtype=torch.int32, device=dev)
+        npp = torch.empty(1, dtype=torch.int32, device=dev)
+        counts = torch.empty(E, dtype=torch.int32, device=dev) if with_counts else None
+    else:
+        sorted_ids, expert_ids, npp, counts = out
+    if status is not None:
+        _check(status, "status", torch.int32, device=dev)
+    st = load().wna16_moe_align_block_size(_ptr(topk_ids), M, topk, E, block, _ptr(sorted_ids),
+                                           _ptr(expert_ids), _ptr(npp), _ptr(counts), _ptr(status),
+                                           _stream(stream))
+    _raise(st, "wna16_moe_align_block_size")
+    return sorted_ids[:cap], expert_ids[: cap // block], npp, counts
+
+
+def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tensor,
+              w13_zeros: Optional[torch.Tensor], w2_q: torch.Tensor, w2_scales: torch.Tensor,
+              w2_zeros: Optional[torch.Tensor], topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+              bits: int, group_size: int, out: Optional[torch.Tensor] = None,
+              workspace: Optional[torch.Tensor] = None, block: int = 0, split_k: int = 0,
+              stream=None) -> torch.Tensor:
+    """The fused layer (see include/wna16_moe.h). Returns ``out`` [M, H]."""
+    _check(hidden, "hidden", (torch.float16, torch.bfloat16))
+    dev = hidden.device
+    M, H = hidden.shape
+    E, twoI, kw = w13_q.shape
+    I = twoI // 2
+    pf = 32 // bits
+    G1 = H if group_size == -1 else group_size
+    G2 = I if group_size == -1 else group_size
+    _check(w13_q, "w13_q", torch.int32, (E, 2 * I, H // pf), dev)
+    _check(w2_q, "w2_q", torch.int32, (E, H, I // pf), dev)
+    _check(w13_scales, "w13_scales", (torch.float16, torch.bfloat16), (E, H // G1, 2 * I), dev)
+    _check(w2_scales, "w2_scales", w13_scales.dtype, (E, I // G2, H), dev)
+    if (w13_zeros is None) != (w2_zeros is None):
+        raise ValueError("w13_zeros and w2_zeros must both be given or both be None")
+    if w13_zeros is not None:
+        _check(w13_zeros, "w13_zeros", torch.int32, (E, H // G1, 2 * I // pf), dev)
+        _check(w2_zeros, "w2_zeros", torch.int32, (E, I // G2, H // pf), dev)
+    _check(topk_ids, "topk_ids", torch.int32, device=dev)
+    topk = topk_ids.shape[1] if topk_ids.dim() == 2 else -1
+    _check(topk_ids, "topk_ids", torch.int32, (M, topk), dev)
+    _check(topk_weights, "topk_weights", torch.float32, (M, topk), dev)
+    if out is None:
+        out = torch.empty_like(hidden)
+    _check(out, "out", hidden.dtype, (M, H), dev)
+    need = workspace_bytes(M, H, I, E, topk, bits, group_size, block, split_k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", torch.uint8, device=dev)
+    st = load().wna16_fused_moe(
+        _ptr(hidden), _DTYPE[hidden.dtype], M, H, I, E, topk, _ptr(w13_q), _ptr(w13_scales),
+        _ptr(w13_zeros), _ptr(w2_q), _ptr(w2_scales), _ptr(w2_zeros), _DTYPE[w13_scales.dtype], bits,
+        group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out), _ptr(workspace),
+        workspace.numel(), block, split_k, _stream(stream))
+    _raise(st, "wna16_fused_moe")
+    return out
+
+
+def read_device_status(status_word: torch.Tensor, stream=None) -> int:
+    """Synchronizes the stream and returns the raw device status bits."""
+    bits = ctypes.c_int32(0)
+    st = load().wna16_read_device_status(_ptr(status_word), ctypes.byref(bits), _stream(stream))
+    if st not in (0, 5, 6):
+        _raise(st, "wna16_read_device_status")
+    return int(bits.value)

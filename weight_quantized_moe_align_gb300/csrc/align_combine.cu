@@ -1,0 +1,209 @@
+// moe_align_block_size and the ordered top-k combine.
+//
+// Align (vLLM PR #12185, note 1: a shared-memory align kernel that supports
+// DeepSeek-V3's 256 experts and CUDA graphs): one CTA of 1024 threads.
+//   1. histogram of expert ids in shared memory;
+//   2. exclusive scan of the block-padded counts (one warp, 8 experts/lane);
+//   3. sentinel fill of sorted_ids, expert id of every block by binary search;
+//   4. stable scatter, 1024 pairs per round: __match_any_sync gives each pair
+//      its rank among same-expert lanes of its warp, a per-expert scan over the
+//      32 warps gives the warp's base, so the order within an expert is the
+//      pair order (deterministic, no atomics on the output).
+// All sizes are fixed by the capacity bound, so the launch never depends on
+// data read back to the host.
+//
+// Combine: out[t, h] = sum over slots j (in slot order) of the down GEMM's fp32
+// rows (already scaled by the top-k weight; one row per K split), rounded once
+// to the activation dtype. Each output element is written by one thread; no
+// atomics.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace wna16 {
+
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kMaxExperts = 256;
+
+__global__ void __launch_bounds__(kAlignThreads, 1)
+    moe_align_kernel(const int32_t* __restrict__ ids, int P, int E, int block, int cap,
+                     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                     int32_t* __restrict__ num_post_pad, int32_t* __restrict__ counts_out,
+                     int32_t* __restrict__ status) {
+  __shared__ int cnt[kMaxExperts];
+  __shared__ int off_end[kMaxExperts];      // exclusive end of each expert's padded segment
+  __shared__ int run[kMaxExperts];          // next free slot of each expert
+  __shared__ int wbase[kAlignWarps][kMaxExperts];
+  __shared__ int total;
+  __shared__ int bad;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid < kMaxExperts) cnt[tid] = 0;
+  for (int i = tid; i < kAlignWarps * kMaxExperts; i += kAlignThreads) (&wbase[0][0])[i] = 0;
+  if (tid == 0) bad = 0;
+  if (tid == 0 && status) *status = 0;
+  __syncthreads();
+
+  // 1. histogram
+  for (int p = tid; p < P; p += kAlignThreads) {
+    const int e = ids[p];
+    if (e >= 0 && e < E)
+      atomicAdd(&cnt[e], 1);
+    else
+      bad = 1;
+  }
+  __syncthreads();
+
+  // 2. scan of padded counts (warp 0; lane l owns experts 8l .. 8l+7)
+  if (warp == 0) {
+    int pad[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      const int c = e < E ? cnt[e] : 0;
+      pad[i] = (c + block - 1) / block * block;
+      sum += pad[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int start = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < kMaxExperts) {
+        run[e] = start;
+        start += pad[i];
+        off_end[e] = start;
+      }
+    }
+    if (lane == 31) total = incl;
+  }
+  __syncthreads();
+  const int npp = total;
+  if (tid == 0) {
+    *num_post_pad = npp;
+    if (status && bad) atomicOr(status, 0x1 /* WNA16_DEV_BAD_EXPERT_ID */);
+  }
+  if (counts_out)
+    for (int e = tid; e < E; e += kAlignThreads) counts_out[e] = cnt[e];
+
+  // 3. sentinel fill and per-block expert ids
+  for (int i = tid; i < cap; i += kAlignThreads) sorted_ids[i] = P;
+  const int nblk = cap / block;
+  for (int b = tid; b < nblk; b += kAlignThreads) {
+    const int start = b * block;
+    int e = -1;
+    if (start < npp) {  // first expert whose padded segment ends after `start`
+      int lo = 0, hi = E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (off_end[mid] > start)
+          hi = mid;
+        else
+          lo = mid + 1;
+      }
+      e = lo;
+    }
+    expert_ids[b] = e;
+  }
+  __syncthreads();  // orders the sentinel fill before the scatter below
+
+  // 4. stable scatter
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = 0; base < P; base += kAlignThreads) {
+    const int p = base + tid;
+    int e = p < P ? ids[p] : -1;
+    const bool valid = e >= 0 && e < E;
+    if (!valid) e = -1;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank = __popc(peers & lt_mask);
+    const bool leader = (__ffs(peers) - 1) == lane;
+    if (valid && leader) wbase[warp][e] = __popc(peers);
+    __syncthreads();
+    // per-expert exclusive scan across warps (in warp order = pair order)
+    for (int x = tid; x < E; x += kAlignThreads) {
+      int r = run[x];
+#pragma unroll 4
+      for (int w = 0; w < kAlignWarps; ++w) {
+        const int c = wbase[w][x];
+        wbase[w][x] = r;
+        r += c;
+      }
+      run[x] = r;
+    }
+    __syncthreads();
+    if (valid) sorted_ids[wbase[warp][e] + rank] = p;
+    __syncthreads();
+    for (int x = tid; x < E; x += kAlignThreads)
+      for (int w = 0; w < kAlignWarps; ++w) wbase[w][x] = 0;
+    __syncthreads();
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// One thread per 4 consecutive outputs of one token.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    moe_combine_kernel(const float* __restrict__ slab, const int32_t* __restrict__ ids, int M, int H,
+                       int topk, int E, int split, T* __restrict__ out) {
+  const int h4 = H / 4;
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<long long>(M) * h4) return;
+  const int t = static_cast<int>(idx / h4);
+  const int h = static_cast<int>(idx % h4) * 4;
+  const long long P = static_cast<long long>(M) * topk;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < topk; ++j) {
+    const int e = ids[t * topk + j];
+    if (e < 0 || e >= E) continue;  // dropped pair
+    for (int s = 0; s < split; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(slab + ((s * P) + t * topk + j) * H + h);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+  }
+  T o[4] = {from_f32<T>(acc.x), from_f32<T>(acc.y), from_f32<T>(acc.z), from_f32<T>(acc.w)};
+  *reinterpret_cast<uint2*>(out + static_cast<long long>(t) * H + h) = *reinterpret_cast<uint2*>(o);
+}
+
+cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, int32_t* sorted_ids,
+                         int32_t* expert_ids, int32_t* num_post_pad, int32_t* counts,
+                         int32_t* status, cudaStream_t stream) {
+  moe_align_kernel<<<1, kAlignThreads, 0, stream>>>(ids, P, E, block, cap, sorted_ids, expert_ids,
+                                                    num_post_pad, counts, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* slab, const int32_t* ids, int M, int H, int topk, int E,
+                           int split, int act_dtype, void* out, cudaStream_t stream) {
+  const long long n = static_cast<long long>(M) * (H / 4);
+  const int threads = 256;
+  const unsigned blocks = static_cast<unsigned>((n + threads - 1) / threads);
+  if (act_dtype == 0)
+    moe_combine_kernel<__half><<<blocks, threads, 0, stream>>>(slab, ids, M, H, topk, E, split,
+                                                               static_cast<__half*>(out));
+  else
+    moe_combine_kernel<__nv_bfloat16><<<blocks, threads, 0, stream>>>(
+        slab, ids, M, H, topk, E, split, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace wna16

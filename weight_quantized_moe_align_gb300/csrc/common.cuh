@@ -1,0 +1,78 @@
+// Shared definitions of the host layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace wna16 {
+
+// Threads of the grouped-GEMM kernel and their roles (warp index):
+//   0      TMA producer (packed weights, scales, zero points)
+//   1      tcgen05 MMA issuer, owner of the TMEM allocation
+//   2..3   activation gatherers (cp.async rows of the token tile)
+//   4..7   epilogue (TMEM -> registers -> global)
+//   8..15  dequantizers (shared -> registers -> TMEM A operand)
+constexpr int kGemmThreads = 512;
+constexpr int kLoaderThreads = 64;
+constexpr int kDequantWarps = 8;
+constexpr int kEpilogueWarps = 4;
+
+constexpr int kTileK = 64;       // K elements per pipeline stage
+constexpr int kTileRows = 128;   // weight rows per tile (MMA M)
+constexpr int kGateUpRows = 64;  // gate/up GEMM: 64 gate + 64 up rows per tile
+constexpr int kMaxStages = 24;
+constexpr int kMaxASlots = 8;
+constexpr int kLoaderLag = 4;    // cp.async groups in flight before signalling
+
+struct GemmArgs {
+  const uint8_t* b_src;        // token rows: hidden [M, K] or act cache [cap, K] (16-bit)
+  const int32_t* sorted_ids;   // [cap]
+  const int32_t* expert_ids;   // [cap / block]
+  const int32_t* num_post_pad; // [1]
+  const float* topk_w;         // [P] (down GEMM)
+  void* out;                   // act cache [cap, I] (gate/up) or slab [split, P, H] fp32 (down)
+  int* status;                 // device status word
+  int K;                       // reduction length (H or I)
+  int N;                       // rows of one expert's matrix (2I or H)
+  int I;                       // gate/up GEMM: first up row; down GEMM: unused
+  int E;
+  int n_tiles;                 // weight-row tiles per expert
+  int topk;
+  int P;                       // M * topk
+  int block;                   // align block = token tile (MMA N)
+  int groups;                  // K / G
+  int kt_per_group;            // G / 64
+  int kt_total;                // K / 64
+  int split;                   // K splits (down GEMM), 1 otherwise
+  int has_zeros;
+  int max_blocks;              // cap / block
+  int num_stages;
+  int num_aslots;
+  int num_acc;
+  uint32_t tmem_cols;
+};
+
+// Bytes of one weight stage in shared memory: packed codes of 128 rows x 64 K,
+// then 128 scales (256 B), then the zero-point words (two 128 B slots: the
+// gate/up GEMM loads gate and up zero points separately and every TMA
+// destination must be 128 B aligned). The token ring after the weight ring is 1 KB aligned
+// (128-byte-swizzle atoms).
+__host__ __device__ constexpr int weight_stage_bytes(int bits) {
+  return kTileRows * kTileK * bits / 8 + 256 + 256;
+}
+__host__ __device__ constexpr int weight_ring_bytes(int bits, int stages) {
+  return (stages * weight_stage_bytes(bits) + 1023) / 1024 * 1024;
+}
+__host__ __device__ constexpr int token_stage_bytes(int block) { return block * 128; }
+
+// Fixed extras after the two rings: per-thread loader row tables, barriers, flags.
+__host__ __device__ constexpr int gemm_extra_bytes(int block) {
+  return kLoaderThreads * (block / 8) * 4 + 8 * (3 * kMaxStages + 2 * kMaxASlots + 4 + 1) + 64;
+}
+__host__ __device__ constexpr int gemm_smem_bytes(int bits, int block, int stages) {
+  return 1024 /* base alignment slack */ + weight_ring_bytes(bits, stages) +
+         stages * token_stage_bytes(block) + gemm_extra_bytes(block);
+}
+
+}  // namespace wna16

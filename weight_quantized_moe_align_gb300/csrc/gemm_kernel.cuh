@@ -1,0 +1,471 @@
+// Grouped expert GEMM with in-kernel dequantization of packed int4/int8 weights,
+// on the sm_103a tensor cores (tcgen05, A operand in tensor memory).
+//
+// One launch covers every expert (vLLM PR #12185: one fused launch instead of
+// one GEMM per expert). Work unit = (token block of the align output, tile of
+// weight rows, K split). The token block holds `block` expert-sorted (token,
+// slot) pairs, all routed to the same expert, so one unit is a dense
+//     D[128 rows, block tokens] = Wdeq[128 rows, K] * X[block tokens, K]^T
+// with the dequantized weights as the MMA A operand (M = 128) and the tokens as
+// the B operand (N = block). Swapping the operands this way keeps M = 128 even
+// for a single decode token.
+//
+// Pipeline per CTA (persistent over units; every wait is time-bounded):
+//   TMA warp:      packed weights/scales/zeros of stage s  -> smem ring  (wfull[s])
+//   gather warps:  token rows (cp.async, zero fill for pad) -> smem ring (bfull[s])
+//   dequant warps: smem codes -> fp16/bf16 -> tcgen05.st into a TMEM A slot (afull)
+//   MMA warp:      4 x tcgen05.mma K=16 per stage, commits empty[s], aempty[slot]
+//   epilogue:      TMEM accumulator -> silu(gate)*up -> act cache   (gate/up GEMM)
+//                  TMEM accumulator * topk weight -> fp32 slab row  (down GEMM)
+// Each K stage spans 64 elements and lies inside one quantization group
+// (group size a multiple of 64): the per-stage scale is the scale of the group
+// that K range belongs to (the BLOCK_SIZE_K vs group-size hazard reported on
+// vLLM PR #6502 cannot occur).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace wna16 {
+
+template <int ACT>
+struct Act;
+template <>
+struct Act<0> {
+  using T = __half;
+  using T2 = __half2;
+};
+template <>
+struct Act<1> {
+  using T = __nv_bfloat16;
+  using T2 = __nv_bfloat162;
+};
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+  return d;
+}
+
+template <int ACT>
+__device__ __forceinline__ uint32_t pack2_rn(float lo, float hi) {
+  if constexpr (ACT == 0) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <int ACT>
+__device__ __forceinline__ uint32_t hsub_hmul(uint32_t v, uint32_t zc, uint32_t sc) {
+  using T2 = typename Act<ACT>::T2;
+  T2 r = __hmul2(__hsub2(*reinterpret_cast<T2*>(&v), *reinterpret_cast<T2*>(&zc)),
+                 *reinterpret_cast<T2*>(&sc));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Exact (code - zero) as fp32: 2^23 + code has the code in its low mantissa bits.
+__device__ __forceinline__ float code_minus_zero(uint32_t code, float magic_plus_zero) {
+  return __uint_as_float(0x4B000000u | code) - magic_plus_zero;
+}
+
+// Dequantizes 32 consecutive K elements of one weight row into 16 packed pairs
+// (element 2c in the low half of out[c]). Every value is round((u - z) * s) to
+// the activation dtype, rounded once: the product of a <= 8-bit integer and a
+// 16-bit scale is exact in fp32 and in the half-precision fast paths the
+// subtraction is exact and the multiply rounds once.
+template <int BITS, int ACT, int SCL>
+struct Dequant {
+  static __device__ __forceinline__ void run(const uint32_t* w, uint32_t zero, uint32_t scale_bits,
+                                             uint32_t (&out)[16]) {
+    if constexpr (BITS == 4 && ACT == SCL) {
+      // Magic-exponent conversion: a nibble OR-ed into the mantissa of
+      // 1024.0 (fp16) or 128.0 (bf16) is exactly 1024+u / 128+u.
+      constexpr uint32_t kMagic = ACT == 0 ? 0x64006400u : 0x43004300u;
+      const float base = ACT == 0 ? 1024.f : 128.f;
+      uint32_t zc, sc;
+      {
+        const uint32_t zb = pack2_rn<ACT>(base + float(zero), base + float(zero));
+        zc = zb;
+        sc = (scale_bits & 0xFFFFu) | (scale_bits << 16);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t x = w[i];
+        const uint32_t xs = x >> 4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // byte0 <- low nibble of byte j (element 2j), byte2 <- high nibble (2j+1)
+          const uint32_t t = __byte_perm(x, xs, j | ((j + 4) << 8));
+          out[i * 4 + j] = hsub_hmul<ACT>(lop3_and_or(t, 0x000F000Fu, kMagic), zc, sc);
+        }
+      }
+    } else if constexpr (BITS == 8 && ACT == 0 && SCL == 0) {
+      const uint32_t zc = pack2_rn<0>(1024.f + float(zero), 1024.f + float(zero));
+      const uint32_t sc = (scale_bits & 0xFFFFu) | (scale_bits << 16);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t x = w[i];
+        out[i * 2 + 0] = hsub_hmul<0>(__byte_perm(x, 0x64646464u, 0x4140), zc, sc);
+        out[i * 2 + 1] = hsub_hmul<0>(__byte_perm(x, 0x64646464u, 0x4342), zc, sc);
+      }
+    } else {
+      // General path (int8 with bf16, or scale dtype != activation dtype):
+      // exact (u - z) in fp32, exact product, one rounding to the act dtype.
+      const float s = SCL == 0 ? __half2float(__ushort_as_half((unsigned short)scale_bits))
+                               : __bfloat162float(__ushort_as_bfloat16((unsigned short)scale_bits));
+      const float mz = 8388608.f + float(zero);
+      constexpr int PF = 32 / BITS;
+      constexpr uint32_t MASK = (1u << BITS) - 1;
+#pragma unroll
+      for (int i = 0; i < BITS; ++i) {  // 4 words of int4 or 8 words of int8
+        const uint32_t x = w[i];
+#pragma unroll
+        for (int c = 0; c < PF; c += 2) {
+          const float f0 = code_minus_zero((x >> (BITS * c)) & MASK, mz) * s;
+          const float f1 = code_minus_zero((x >> (BITS * (c + 1))) & MASK, mz) * s;
+          out[(i * PF + c) / 2] = pack2_rn<ACT>(f0, f1);
+        }
+      }
+    }
+  }
+};
+
+struct Unit {
+  int blk, tile, sp, kt0, kt1;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, int nb, const GemmArgs& a) {
+  Unit r;
+  r.blk = u % nb;
+  const int rest = u / nb;
+  r.sp = rest % a.split;
+  r.tile = rest / a.split;
+  r.kt0 = static_cast<int>(static_cast<long long>(a.kt_total) * r.sp / a.split);
+  r.kt1 = static_cast<int>(static_cast<long long>(a.kt_total) * (r.sp + 1) / a.split);
+  return r;
+}
+
+__device__ __forceinline__ int unit_expert(const GemmArgs& a, int blk) {
+  const int e = a.expert_ids[blk];
+  return (e >= 0 && e < a.E) ? e : 0;  // blocks below num_post_pad always hold a valid id
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  int ok = 0;
+  if (lane_id() == 0) ok = wait_bar(bar, parity, abort_flag, status) ? 1 : 0;
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+template <int BITS, int ACT, int SCL, int GEMM>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
+                    const __grid_constant__ CUtensorMap tm_z, const GemmArgs a) {
+  constexpr int PF = 32 / BITS;
+  constexpr int KW = kTileK * BITS / 32;  // int32 words per row per stage
+  constexpr int W_BYTES = kTileRows * KW * 4;
+  constexpr int S_OFF = W_BYTES;
+  constexpr int Z_OFF = W_BYTES + 256;
+  constexpr int WST = weight_stage_bytes(BITS);
+  constexpr uint32_t ZMASK = (1u << BITS) - 1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int NS = a.num_stages, NA = a.num_aslots, NACC = a.num_acc, NT = a.block;
+  const int BST = token_stage_bytes(NT);
+
+  uint8_t* wring = smem;
+  uint8_t* bring = smem + weight_ring_bytes(BITS, NS);
+  int* rowtab = reinterpret_cast<int*>(bring + NS * BST);  // [NT/8][64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rowtab + kLoaderThreads * (NT / 8));
+  uint64_t* wfull = bars;
+  uint64_t* bfull = wfull + NS;
+  uint64_t* empty = bfull + NS;
+  uint64_t* afull = empty + NS;
+  uint64_t* aempty = afull + NA;
+  uint64_t* accfull = aempty + NA;
+  uint64_t* accempty = accfull + NACC;
+  uint64_t* drain = accempty + NACC;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&bfull[s], kLoaderThreads);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < NA; ++i) {
+      mbar_init(&afull[i], kDequantWarps);
+      mbar_init(&aempty[i], 1);
+    }
+    for (int i = 0; i < NACC; ++i) {
+      mbar_init(&accfull[i], 1);
+      mbar_init(&accempty[i], kEpilogueWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_s);
+    if (a.has_zeros) prefetch_tmap(&tm_z);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  int nb = *a.num_post_pad / NT;
+  nb = nb < 0 ? 0 : (nb > a.max_blocks ? a.max_blocks : nb);
+  const int units = nb * a.n_tiles * a.split;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t stage_tx = W_BYTES + 256 + (a.has_zeros ? (kTileRows / PF) * 4 : 0);
+      const uint64_t pol = l2_policy_evict_first();
+      int it = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const Unit w = decode_unit(u, nb, a);
+        const int e = unit_expert(a, w.blk);
+        bool ok = true;
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
+          const int s = it % NS;
+          if (!wait_bar(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&wfull[s], stage_tx);
+          uint8_t* dst = wring + s * WST;
+          const int ys = e * a.groups + kt / a.kt_per_group;
+          if (GEMM == 1) {
+            const int f0 = w.tile * kGateUpRows;
+            tma_load_2d(dst, &tm_q, &wfull[s], kt * KW, e * a.N + f0, pol);
+            tma_load_2d(dst + kGateUpRows * KW * 4, &tm_q, &wfull[s], kt * KW, e * a.N + a.I + f0, pol);
+            tma_load_2d(dst + S_OFF, &tm_s, &wfull[s], f0, ys, pol);
+            tma_load_2d(dst + S_OFF + 128, &tm_s, &wfull[s], a.I + f0, ys, pol);
+            if (a.has_zeros) {
+              tma_load_2d(dst + Z_OFF, &tm_z, &wfull[s], f0 / PF, ys, pol);
+              tma_load_2d(dst + Z_OFF + 128, &tm_z, &wfull[s], (a.I + f0) / PF, ys, pol);
+            }
+          } else {
+            const int r0 = w.tile * kTileRows;
+            tma_load_2d(dst, &tm_q, &wfull[s], kt * KW, e * a.N + r0, pol);
+            tma_load_2d(dst + S_OFF, &tm_s, &wfull[s], r0, ys, pol);
+            if (a.has_zeros) tma_load_2d(dst + Z_OFF, &tm_z, &wfull[s], r0 / PF, ys, pol);
+          }
+        }
+        if (!ok) break;
+      }
+      // Let every issued copy land before the CTA can exit.
+      for (int j = (it > NS ? it - NS : 0); j < it; ++j) wait_bar_drain(&wfull[j % NS], (j / NS) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(ACT, NT);
+      int it = 0, ait = 0, uc = 0;
+      bool issued = false;
+      for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
+        const Unit w = decode_unit(u, nb, a);
+        const int acc = uc % NACC;
+        if (!wait_bar(&accempty[acc], ((uc / NACC) & 1) ^ 1, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * NT;
+        bool ok = true;
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++it, ++ait) {
+          const int s = it % NS;
+          const int slot = ait % NA;
+          if (!wait_bar(&afull[slot], (ait / NA) & 1, abort_flag, a.status) ||
+              !wait_bar(&bfull[s], (it / NS) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_tmem = tmem + NACC * NT + slot * 32;
+          const uint32_t b_addr = smem_u32(bring + s * BST);
+#pragma unroll
+          for (int kk = 0; kk < kTileK / 16; ++kk)
+            mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
+                   (kt > w.kt0 || kk > 0) ? 1u : 0u);
+          mma_commit(&empty[s]);
+          mma_commit(&aempty[slot]);
+          issued = true;
+        }
+        if (!ok) break;
+        mma_commit(&accfull[acc]);
+      }
+      if (issued) {
+        mma_commit(drain);
+        wait_bar_drain(drain, 0);
+      }
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ token gather
+    const int lt = threadIdx.x - 64;
+    const int nrow = NT / 8;  // rows handled by this thread: r = lt/8 + 8*i
+    int it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit w = decode_unit(u, nb, a);
+      for (int i = 0; i < nrow; ++i) {
+        const int r = (lt >> 3) + 8 * i;
+        const int slot = w.blk * NT + r;
+        const int pid = a.sorted_ids[slot];
+        int src = -1;
+        if (pid >= 0 && pid < a.P) src = (GEMM == 1) ? pid / a.topk : slot;
+        rowtab[i * kLoaderThreads + lt] = src;
+      }
+      const int c = lt & 7;
+      bool ok = true;
+      for (int kt = w.kt0; kt < w.kt1; ++kt) {
+        const int s = it % NS;
+        if (!wait_bar(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+        const uint32_t dst = smem_u32(bring + s * BST);
+        for (int i = 0; i < nrow; ++i) {
+          const int r = (lt >> 3) + 8 * i;
+          const int src = rowtab[i * kLoaderThreads + lt];
+          const uint8_t* g = a.b_src + (static_cast<size_t>(src < 0 ? 0 : src) * a.K + kt * kTileK + c * 8) * 2;
+          cp_async_16(dst + r * 128 + ((c ^ (r & 7)) << 4), g, src >= 0 ? 16u : 0u);
+        }
+        cp_async_commit();
+        ++it;
+        if (it > kLoaderLag) {
+          cp_async_wait<kLoaderLag>();
+          fence_proxy_async_smem();
+          mbar_arrive(&bfull[(it - 1 - kLoaderLag) % NS]);
+        }
+      }
+      if (!ok) break;
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (int j = (it > kLoaderLag ? it - kLoaderLag : 0); j < it; ++j) mbar_arrive(&bfull[j % NS]);
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    int uc = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
+      const Unit w = decode_unit(u, nb, a);
+      const int acc = uc % NACC;
+      if (!warp_wait(&accfull[acc], (uc / NACC) & 1, abort_flag, a.status)) break;
+      tc_fence_after();
+      const uint32_t t_base = tmem + ((q * 32) << 16) + acc * NT;
+      for (int c0 = 0; c0 < NT; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(t_base + c0, v);
+        tmem_ld_wait();
+        if (GEMM == 1) {
+          // Lanes 0-15 of this quarter hold gate rows, lanes 16-31 the up rows of
+          // the same 16 features; swap halves so each lane owns 8 (feature, token)
+          // pairs with both values.
+          using T = typename Act<ACT>::T;
+          T* act = reinterpret_cast<T*>(a.out);
+          const bool lo = lane < 16;
+          const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t mine = lo ? v[j] : v[j + 8];
+            const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, lo ? v[j + 8] : v[j], 16);
+            const float g = __uint_as_float(lo ? mine : other);
+            const float up = __uint_as_float(lo ? other : mine);
+            const float silu = g / (1.0f + __expf(-g));
+            const int col = c0 + (lo ? j : j + 8);
+            const size_t row = static_cast<size_t>(w.blk) * NT + col;
+            if constexpr (ACT == 0)
+              act[row * a.I + f] = __float2half_rn(silu * up);
+            else
+              act[row * a.I + f] = __float2bfloat16_rn(silu * up);
+          }
+        } else {
+          float* slab = reinterpret_cast<float*>(a.out);
+          const int h = w.tile * kTileRows + q * 32 + lane;
+          const int my_pid = a.sorted_ids[w.blk * NT + c0 + (lane & 15)];
+          const float my_w = (my_pid >= 0 && my_pid < a.P) ? a.topk_w[my_pid] : 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int pid = __shfl_sync(0xFFFFFFFFu, my_pid, j);
+            const float tw = __shfl_sync(0xFFFFFFFFu, my_w, j);
+            if (pid >= 0 && pid < a.P && h < a.N)
+              slab[(static_cast<size_t>(w.sp) * a.P + pid) * a.N + h] = __uint_as_float(v[j]) * tw;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[acc]);
+    }
+  } else {
+    // ------------------------------------------------------------ dequantizers
+    const int q = warp & 3;
+    const int half = (warp - 8) >> 2;  // which 32-element half of the stage's K
+    int srow;
+    if (GEMM == 1)
+      srow = lane < 16 ? (16 * q + lane) : (kGateUpRows + 16 * q + lane - 16);
+    else
+      srow = q * 32 + lane;
+    const uint32_t t_lane = (q * 32) << 16;
+    int it = 0, ait = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit w = decode_unit(u, nb, a);
+      bool ok = true;
+      for (int kt = w.kt0; kt < w.kt1; ++kt, ++it, ++ait) {
+        const int s = it % NS;
+        const int slot = ait % NA;
+        if (!warp_wait(&wfull[s], (it / NS) & 1, abort_flag, a.status) ||
+            !warp_wait(&aempty[slot], ((ait / NA) & 1) ^ 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* st = wring + s * WST;
+        const uint32_t sbits = reinterpret_cast<const uint16_t*>(st + S_OFF)[srow];
+        uint32_t zero = 1u << (BITS - 1);
+        if (a.has_zeros) {
+          // gate/up: rows [64, 128) are the up rows, their zero words start at +128 B
+          const int zr = (GEMM == 1 && srow >= kGateUpRows) ? srow - kGateUpRows : srow;
+          const uint8_t* zbase = st + Z_OFF + ((GEMM == 1 && srow >= kGateUpRows) ? 128 : 0);
+          zero = (reinterpret_cast<const uint32_t*>(zbase)[zr / PF] >> (BITS * (zr % PF))) & ZMASK;
+        }
+        uint32_t wv[BITS];  // 32 K elements = BITS words
+        const uint4* src = reinterpret_cast<const uint4*>(st + srow * KW * 4 + half * BITS * 4);
+#pragma unroll
+        for (int i = 0; i < BITS / 4; ++i) {
+          const uint4 x = src[i];
+          wv[4 * i + 0] = x.x;
+          wv[4 * i + 1] = x.y;
+          wv[4 * i + 2] = x.z;
+          wv[4 * i + 3] = x.w;
+        }
+        uint32_t outv[16];
+        Dequant<BITS, ACT, SCL>::run(wv, zero, sbits, outv);
+        tmem_st16(tmem + t_lane + NACC * NT + slot * 32 + half * 16, outv);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[slot]);
+      }
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, a.tmem_cols);
+  }
+}
+
+}  // namespace wna16

@@ -1,0 +1,361 @@
+// C ABI of the fused weight-quantized MoE layer: argument checks, workspace
+// layout, block/split heuristics, TMA descriptors and the launch sequence
+// align -> gate/up GEMM -> down GEMM -> combine (all on the caller's stream,
+// no host synchronization, no allocation).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/wna16_moe.h"
+#include "common.cuh"
+#include "gemm_launch.cuh"
+
+using namespace wna16;
+
+namespace {
+
+constexpr int kMaxSmem = 232448;  // opt-in dynamic shared memory per CTA on sm_103a
+constexpr int kMinSmem = 120 * 1024;  // keeps one GEMM CTA per SM (TMEM is not shared)
+
+bool is_pow2(long long v) { return v > 0 && (v & (v - 1)) == 0; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int64_t capacity(int64_t P, int E, int block) {
+  const int64_t raw = P + std::min<int64_t>(P, E) * (block - 1);
+  return (raw + block - 1) / block * block;
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  static int cache[64] = {};
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+int choose_block_impl(int64_t M, int topk, int E) {
+  const int64_t P = M * topk;
+  if (P <= 0) return 16;
+  const int64_t active = std::min<int64_t>(P, E);
+  const int64_t avg = (P + active - 1) / active;  // pairs per active expert
+  int b = 16;
+  while (b < 128 && b < avg) b <<= 1;
+  return b;
+}
+
+// Pipeline shape of one GEMM launch for a token tile of `block`.
+struct Pipe {
+  int stages, aslots, acc;
+  uint32_t tmem_cols;
+  size_t smem;
+};
+
+Pipe pipe_for(int bits, int block) {
+  Pipe p;
+  p.acc = block <= 128 ? 2 : 1;
+  p.aslots = std::min(kMaxASlots, (512 - p.acc * block) / 32);
+  const int need = p.acc * block + p.aslots * 32;
+  p.tmem_cols = 32;
+  while (static_cast<int>(p.tmem_cols) < need) p.tmem_cols <<= 1;
+  p.stages = kMaxStages;
+  while (p.stages > 2 && gemm_smem_bytes(bits, block, p.stages) > kMaxSmem) --p.stages;
+  p.smem = std::max<size_t>(gemm_smem_bytes(bits, block, p.stages), kMinSmem);
+  return p;
+}
+
+int choose_split(int64_t units, int kt_total) {
+  const int sms = sm_count();
+  if (units >= sms) return 1;
+  int s = static_cast<int>(sms / std::max<int64_t>(units, 1));
+  s = std::min(s, 8);
+  s = std::min(s, std::max(1, kt_total / 8));  // keep >= 8 K stages per split
+  return std::max(s, 1);
+}
+
+struct WsLayout {
+  size_t status, sorted, experts, npp, counts, act, slab, total;
+};
+
+WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, int split) {
+  const int64_t P = M * topk;
+  const int64_t cap = capacity(P, E, block);
+  WsLayout w;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t r = o;
+    o = align_up(o + bytes, 256);
+    return r;
+  };
+  w.status = take(4);
+  w.sorted = take(static_cast<size_t>(cap) * 4);
+  w.experts = take(static_cast<size_t>(cap / block) * 4);
+  w.npp = take(4);
+  w.counts = take(static_cast<size_t>(E) * 4);
+  w.act = take(static_cast<size_t>(cap) * I * 2);
+  w.slab = take(static_cast<size_t>(split) * P * H * 4);
+  w.total = o;
+  return w;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D tiled map over a row-major [rows, cols] array, box {box_cols, box_rows}.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t cols,
+              uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * elem_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct GemmMaps {
+  CUtensorMap q, s, z;
+};
+
+// Maps of one projection: q [E*N, K/pf] int32, scales [E*K/G, N], zeros [E*K/G, N/pf].
+bool make_gemm_maps(GemmMaps* g, const int32_t* q, const void* s, const int32_t* z, int E, int64_t N,
+                    int64_t K, int G, int bits, uint32_t box_rows) {
+  const int pf = 32 / bits;
+  const int64_t groups = K / G;
+  std::memset(g, 0, sizeof(*g));
+  if (!make_map(&g->q, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, q, K / pf, E * N, kTileK / pf, box_rows))
+    return false;
+  if (!make_map(&g->s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, s, N, E * groups, box_rows, 1)) return false;
+  if (z && !make_map(&g->z, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, z, N / pf, E * groups, box_rows / pf, 1))
+    return false;
+  return true;
+}
+
+cudaError_t launch_gemm(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t st,
+                        const GemmMaps& m, const GemmArgs& a) {
+  return bits == 4 ? launch_gemm_w4(act, scl, gemm, grid, smem, st, m.q, m.s, m.z, a)
+                   : launch_gemm_w8(act, scl, gemm, grid, smem, st, m.q, m.s, m.z, a);
+}
+
+struct Resolved {
+  int block, split, G1, G2;
+};
+
+wna16_status resolve(int64_t M, int64_t H, int64_t I, int E, int topk, int bits, int group_size,
+                     int block, int split_k, Resolved* r) {
+  if (M < 0 || H <= 0 || I <= 0 || E < 1 || topk < 1) return WNA16_ERR_INVALID_ARG;
+  if (E > 256 || topk > E) return WNA16_ERR_UNSUPPORTED;
+  if (bits != 4 && bits != 8) return WNA16_ERR_UNSUPPORTED;
+  if (M * topk >= (int64_t(1) << 31)) return WNA16_ERR_UNSUPPORTED;
+  if (H % 64 || I % 64) return WNA16_ERR_UNSUPPORTED;
+  if (H >= (int64_t(1) << 24) || I >= (int64_t(1) << 24)) return WNA16_ERR_UNSUPPORTED;
+  if (group_size == -1) {
+    r->G1 = static_cast<int>(H);
+    r->G2 = static_cast<int>(I);
+  } else {
+    if (group_size <= 0) return WNA16_ERR_INVALID_ARG;
+    if (group_size % 64 || H % group_size || I % group_size) return WNA16_ERR_UNSUPPORTED;
+    r->G1 = r->G2 = group_size;
+  }
+  if (block == 0) block = choose_block_impl(M, topk, E);
+  if (!is_pow2(block) || block < 16 || block > 256) return WNA16_ERR_INVALID_ARG;
+  r->block = block;
+  if (split_k < 0 || split_k > 8) return WNA16_ERR_INVALID_ARG;
+  const int kt2 = static_cast<int>(I / kTileK);
+  if (split_k == 0) {
+    const int64_t blocks = capacity(M * topk, E, block) / block;
+    const int64_t units = blocks * ((H + kTileRows - 1) / kTileRows);
+    split_k = choose_split(units, kt2);
+  }
+  r->split = std::min(split_k, kt2);
+  return WNA16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t wna16_align_capacity(int64_t num_pairs, int E, int block) {
+  if (num_pairs < 0 || E < 1 || block < 1) return -1;
+  return capacity(num_pairs, E, block);
+}
+
+int wna16_choose_block(int64_t M, int topk, int E) { return choose_block_impl(M, topk, E); }
+
+wna16_status wna16_moe_align_block_size(const int32_t* topk_ids, int64_t M, int topk, int E, int block,
+                                        int32_t* sorted_ids, int32_t* expert_ids,
+                                        int32_t* num_tokens_post_padded, int32_t* expert_counts,
+                                        int32_t* device_status, void* stream) {
+  if (M < 0 || topk < 1 || E < 1) return WNA16_ERR_INVALID_ARG;
+  if (E > 256) return WNA16_ERR_UNSUPPORTED;
+  if (!is_pow2(block) || block < 16 || block > 256) return WNA16_ERR_INVALID_ARG;
+  const int64_t P = M * topk;
+  if (P >= (int64_t(1) << 31)) return WNA16_ERR_UNSUPPORTED;
+  if ((P > 0 && !topk_ids) || !sorted_ids || !expert_ids || !num_tokens_post_padded)
+    return WNA16_ERR_INVALID_ARG;
+  const int64_t cap = capacity(P, E, block);
+  if (launch_align(topk_ids, static_cast<int>(P), E, block, static_cast<int>(cap), sorted_ids, expert_ids,
+                   num_tokens_post_padded, expert_counts, device_status,
+                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return WNA16_ERR_CUDA;
+  return WNA16_OK;
+}
+
+size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, int topk, int bits,
+                                       int group_size, int block, int split_k) {
+  Resolved r;
+  if (resolve(M, H, I, E, topk, bits, group_size, block, split_k, &r) != WNA16_OK) return 0;
+  return ws_layout(M, H, I, E, topk, r.block, r.split).total;
+}
+
+wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I,
+                             int E, int topk, const int32_t* w13_q, const void* w13_scales,
+                             const int32_t* w13_zeros, const int32_t* w2_q, const void* w2_scales,
+                             const int32_t* w2_zeros, wna16_dtype scale_dtype, int bits, int group_size,
+                             const int32_t* topk_ids, const float* topk_weights, void* out,
+                             void* workspace, size_t workspace_bytes, int block, int split_k,
+                             void* stream) {
+  if (act_dtype != WNA16_F16 && act_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
+  if (scale_dtype != WNA16_F16 && scale_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
+  Resolved r;
+  const wna16_status st = resolve(M, H, I, E, topk, bits, group_size, block, split_k, &r);
+  if (st != WNA16_OK) return st;
+  if (M == 0) return WNA16_OK;
+  if (!hidden || !w13_q || !w13_scales || !w2_q || !w2_scales || !topk_ids || !topk_weights || !out ||
+      !workspace)
+    return WNA16_ERR_INVALID_ARG;
+  if ((w13_zeros == nullptr) != (w2_zeros == nullptr)) return WNA16_ERR_INVALID_ARG;
+  const void* ptrs[] = {hidden, w13_q, w13_scales, w13_zeros, w2_q, w2_scales, w2_zeros, out, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return WNA16_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_weights) & 3u))
+    return WNA16_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(M, H, I, E, topk, r.block, r.split);
+  if (workspace_bytes < L.total) return WNA16_ERR_WORKSPACE_TOO_SMALL;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+  int32_t* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+  int32_t* experts = reinterpret_cast<int32_t*>(ws + L.experts);
+  int32_t* npp = reinterpret_cast<int32_t*>(ws + L.npp);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  void* act = ws + L.act;
+  float* slab = reinterpret_cast<float*>(ws + L.slab);
+
+  const int P = static_cast<int>(M * topk);
+  const int B = r.block;
+  const int64_t cap = capacity(P, E, B);
+  const int max_blocks = static_cast<int>(cap / B);
+  const bool zeros = w13_zeros != nullptr;
+
+  if (launch_align(topk_ids, P, E, B, static_cast<int>(cap), sorted, experts, npp, counts, status, s) !=
+      cudaSuccess)
+    return WNA16_ERR_CUDA;
+
+  GemmMaps m1, m2;
+  if (!make_gemm_maps(&m1, w13_q, w13_scales, zeros ? w13_zeros : nullptr, E, 2 * I, H, r.G1, bits,
+                      kGateUpRows) ||
+      !make_gemm_maps(&m2, w2_q, w2_scales, zeros ? w2_zeros : nullptr, E, H, I, r.G2, bits, kTileRows))
+    return WNA16_ERR_CUDA;
+
+  const Pipe pipe = pipe_for(bits, B);
+  const int sms = sm_count();
+
+  GemmArgs a1{};
+  a1.b_src = static_cast<const uint8_t*>(hidden);
+  a1.sorted_ids = sorted;
+  a1.expert_ids = experts;
+  a1.num_post_pad = npp;
+  a1.topk_w = topk_weights;
+  a1.out = act;
+  a1.status = status;
+  a1.K = static_cast<int>(H);
+  a1.N = static_cast<int>(2 * I);
+  a1.I = static_cast<int>(I);
+  a1.E = E;
+  a1.n_tiles = static_cast<int>(I / kGateUpRows);
+  a1.topk = topk;
+  a1.P = P;
+  a1.block = B;
+  a1.groups = static_cast<int>(H / r.G1);
+  a1.kt_per_group = r.G1 / kTileK;
+  a1.kt_total = static_cast<int>(H / kTileK);
+  a1.split = 1;
+  a1.has_zeros = zeros ? 1 : 0;
+  a1.max_blocks = max_blocks;
+  a1.num_stages = pipe.stages;
+  a1.num_aslots = pipe.aslots;
+  a1.num_acc = pipe.acc;
+  a1.tmem_cols = pipe.tmem_cols;
+  const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles;
+  const dim3 grid1(static_cast<unsigned>(std::min<int64_t>(units1, sms)));
+  if (launch_gemm(bits, act_dtype, scale_dtype, 1, grid1, pipe.smem, s, m1, a1) != cudaSuccess)
+    return WNA16_ERR_CUDA;
+
+  GemmArgs a2 = a1;
+  a2.b_src = static_cast<const uint8_t*>(act);
+  a2.out = slab;
+  a2.K = static_cast<int>(I);
+  a2.N = static_cast<int>(H);
+  a2.I = 0;
+  a2.n_tiles = static_cast<int>((H + kTileRows - 1) / kTileRows);
+  a2.groups = static_cast<int>(I / r.G2);
+  a2.kt_per_group = r.G2 / kTileK;
+  a2.kt_total = static_cast<int>(I / kTileK);
+  a2.split = r.split;
+  const int64_t units2 = static_cast<int64_t>(max_blocks) * a2.n_tiles * a2.split;
+  const dim3 grid2(static_cast<unsigned>(std::min<int64_t>(units2, sms)));
+  if (launch_gemm(bits, act_dtype, scale_dtype, 2, grid2, pipe.smem, s, m2, a2) != cudaSuccess)
+    return WNA16_ERR_CUDA;
+
+  if (launch_combine(slab, topk_ids, static_cast<int>(M), static_cast<int>(H), topk, E, r.split,
+                     act_dtype, out, s) != cudaSuccess)
+    return WNA16_ERR_CUDA;
+  return WNA16_OK;
+}
+
+wna16_status wna16_read_device_status(const void* status_word, int32_t* bits_out, void* stream) {
+  if (!status_word) return WNA16_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, status_word, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return WNA16_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return WNA16_ERR_CUDA;
+  if (bits_out) *bits_out = v;
+  if (v & WNA16_DEV_TIMEOUT) return WNA16_ERR_DEVICE_TIMEOUT;
+  if (v & WNA16_DEV_BAD_EXPERT_ID) return WNA16_ERR_DEVICE_BAD_EXPERT_ID;
+  return WNA16_OK;
+}
+
+const char* wna16_status_string(wna16_status status) {
+  switch (status) {
+    case WNA16_OK: return "ok";
+    case WNA16_ERR_INVALID_ARG: return "invalid argument";
+    case WNA16_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case WNA16_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case WNA16_ERR_CUDA: return "CUDA call failed";
+    case WNA16_ERR_DEVICE_BAD_EXPERT_ID: return "device: expert id out of range (pair dropped)";
+    case WNA16_ERR_DEVICE_TIMEOUT: return "device: pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"
