@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""Benchmark of the fused W4A16 / W8A16 MoE layer on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--M M]
+    python bench.py --impl reference ...     # the float64 CPU oracle, same metric
+
+One step = one call of the whole layer (align -> gate/up GEMM -> down GEMM ->
+combine) on one batch of M synthetic tokens with the weights resident in HBM.
+L2 is flushed (a 512 MiB memset, more than twice the 129 MB L2) before every
+step, outside the timed events. Each step's kernels are timed with CUDA events
+on the launching stream; the dominant kernel's launches are timed the same way
+for the roofline. The JSON line also carries an end-to-end number through the
+public API with pinned host buffers and host<->device copies in the timed
+region, the M sweep of the workload, sampled SM clocks, and the oracle timed on
+a bounded sample of the same workload on the host cores.
+
+Multi-GPU (torchrun): every rank runs an independent replica (the layer is
+data-parallel over tokens; no collective on the data path); value = tokens of
+all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synthetic import WORKLOADS, make_expert_weights, make_layer_inputs  # noqa: E402
+from synthetic.workloads import make_routing  # noqa: E402
+
+METRIC = "fused W4A16 MoE layer tokens/s and achieved HBM GB/s (% of peak) vs batch M"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+KERNEL_SOURCES = ("gemm_kernel.cuh", "common.cuh", "ptx.cuh", "host.cu")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="mixtral8x7b", choices=list(WORKLOADS))
+    p.add_argument("--M", type=int, default=16)
+    p.add_argument("--sweep-steps", type=int, default=40)
+    p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work (what the layer must move / compute, not what it executes)
+# ----------------------------------------------------------------------------
+
+def matrix_bytes(wl, N, K):
+    G = wl.G(K)
+    b = N * K * wl.bits // 8 + (K // G) * N * 2
+    if wl.has_zeros:
+        b += (K // G) * N * wl.bits // 8
+    return b
+
+
+def algorithmic(wl, M, ids_np):
+    """Bytes and flops of one layer call, per kernel and whole."""
+    touched = int(np.unique(ids_np[(ids_np >= 0) & (ids_np < wl.E)]).size) if ids_np.size else 0
+    P = M * wl.topk
+    w13 = touched * matrix_bytes(wl, 2 * wl.I, wl.H)
+    w2 = touched * matrix_bytes(wl, wl.H, wl.I)
+    act = M * wl.H * 2
+    return dict(
+        touched=touched,
+        gemm1_bytes=w13 + act, gemm2_bytes=w2,
+        gemm1_flops=2 * P * 2 * wl.I * wl.H, gemm2_flops=2 * P * wl.H * wl.I,
+        layer_bytes=w13 + w2 + 2 * act + P * 8,
+        layer_flops=6 * P * wl.H * wl.I,
+    )
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_hash():
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "weight_quantized_moe_align_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(workload_key, kernel):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel sources
+    still hash to the ones the counters were taken on (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d["entries"][f"{workload_key}/{kernel}"]
+        return float(e["dram_bytes_per_launch"]) if e["kernel_hash"] == kernel_hash() else None
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except Exception:
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the oracle on a bounded sample (CPU baseline and the reference arm)
+# ----------------------------------------------------------------------------
+
+def sample_layer(li, tokens, F):
+    """Oracle inputs for the first ``tokens`` tokens and the first F intermediate
+    features of every expert they route to: a smaller layer of the same kind
+    (the oracle's cost is linear in tokens x F). Pure slicing, no arithmetic."""
+    from tests.helpers import halfbits
+
+    wl = li.wl
+    I, pf = wl.I, wl.pf
+    ids = li.topk_ids[:tokens].cpu()
+    experts = sorted(set(int(e) for e in ids.flatten().tolist() if 0 <= e < wl.E))
+    remap = {e: i for i, e in enumerate(experts)}
+    ex = torch.tensor(experts, dtype=torch.long, device=li.w13_q.device)
+
+    def pick(t):
+        return None if t is None else t.index_select(0, ex)
+
+    q13 = pick(li.w13_q)
+    q13 = torch.cat([q13[:, :F], q13[:, I:I + F]], dim=1)
+    s13 = pick(li.w13_s)
+    s13 = torch.cat([s13[:, :, :F], s13[:, :, I:I + F]], dim=2)
+    z13 = pick(li.w13_z)
+    if z13 is not None:
+        z13 = torch.cat([z13[:, :, :F // pf], z13[:, :, I // pf:(I + F) // pf]], dim=2)
+    n_g2 = 1 if wl.group_size == -1 else F // wl.group_size
+    q2 = pick(li.w2_q)[:, :, :F // pf]
+    s2 = pick(li.w2_s)[:, :n_g2]
+    z2 = pick(li.w2_z)
+    if z2 is not None:
+        z2 = z2[:, :n_g2]
+    np_ = lambda t: None if t is None else t.contiguous().cpu().numpy()
+    return dict(
+        x=halfbits(li.hidden[:tokens]), act_dtype=wl.act_dtype,
+        w13_q=np_(q13), w13_s=halfbits(s13.contiguous()), w13_z=np_(z13),
+        w2_q=np_(q2), w2_s=halfbits(s2.contiguous()), w2_z=np_(z2),
+        scale_dtype=wl.scale_dtype, bits=wl.bits, group_size=wl.group_size,
+        topk_ids=np.array([[remap.get(int(e), -1) for e in row] for row in ids.tolist()], dtype=np.int32),
+        topk_w=li.topk_w[:tokens].cpu().numpy(),
+    )
+
+
+def time_oracle(li, target_s, max_tokens=1):
+    """Times oracle.fused_moe_grouped on a sample sized to about ``target_s``
+    seconds; returns (tokens/s, description, seconds)."""
+    import oracle
+
+    wl = li.wl
+    unit = 64 if wl.group_size == -1 else max(64, wl.group_size)
+    F = unit
+    t0 = time.perf_counter()
+    oracle.fused_moe_grouped(sample_layer(li, 1, F))
+    dt = max(time.perf_counter() - t0, 1e-4)
+    scale = target_s / dt
+    F = int(min(wl.I, max(unit, int(F * scale) // unit * unit)))
+    tokens = 1
+    if F == wl.I:
+        tokens = int(max(1, min(max_tokens, scale * unit / wl.I)))
+    L = sample_layer(li, tokens, F)
+    t0 = time.perf_counter()
+    oracle.fused_moe_grouped(L)
+    dt = time.perf_counter() - t0
+    desc = (f"first {tokens} token(s) x first {F} of I={wl.I} intermediate features of each routed expert "
+            f"(work {tokens * F / wl.I:.4f} tokens)")
+    return tokens * F / wl.I / dt, desc, dt
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+
+def workload_label(wl, M):
+    q = f"int{wl.bits} {'asym' if wl.has_zeros else 'sym'} g{wl.group_size if wl.group_size > 0 else 'channel'}"
+    return (f"{wl.name}: H={wl.H} I={wl.I} E={wl.E} top{wl.topk} {wl.routing}, {q}, "
+            f"{wl.act_dtype} act, {wl.scale_dtype} scales, M={M}")
+
+
+def reference_arm(args):
+    """The oracle as it stands, on the host cores, on a bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = WORKLOADS[args.workload]
+    M = args.M
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    li = make_layer_inputs(wl, M, dev, weights=_sample_weights(wl, M, dev, tokens=4))
+    per_step = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    rates, desc = [], ""
+    for i in range(args.warmup + args.steps):
+        r, desc, _ = time_oracle(li, per_step, max_tokens=4)
+        if i >= args.warmup:
+            rates.append(r)
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * M / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_label(wl, M), "M": M},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def _sample_weights(wl, M, dev, tokens):
+    """Weights of the experts the first ``tokens`` tokens route to (same seeds as
+    the full layer); the other experts are left unset (never read)."""
+    from synthetic.workloads import _seed
+
+    ids, _ = make_routing(wl, M, _seed(wl.name, "route", 1000 + M))
+    used = sorted(set(int(e) for e in ids[:tokens].flatten().tolist()))
+    return make_expert_weights(wl, dev, experts=used)
+
+
+def new_events(steps):
+    """Timing events for ``steps`` steps (6 per step). torch creates a CUDA event
+    on its first record, so each is recorded once here; the library then
+    records them on the launching stream between its launches."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for row in evs:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    return evs
+
+
+def run_steps(call, flush, steps, ev_sets):
+    for i in range(steps):
+        flush.zero_()
+        call(ev_sets[i] if ev_sets is not None else None)
+
+
+def ours_arm(args):
+    import weight_quantized_moe_align_gb300 as w
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w.build()
+    w.load()
+    wl = WORKLOADS[args.workload]
+    M = args.M
+    peaks = load_peaks()
+
+    weights = make_expert_weights(wl, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def setup(Mx):
+        li = make_layer_inputs(wl, Mx, dev, weights)
+        ws = torch.empty(max(16, w.workspace_bytes(Mx, wl.H, wl.I, wl.E, wl.topk, wl.bits, wl.group_size)),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty(Mx, wl.H, dtype=li.hidden.dtype, device=dev)
+
+        def call(events):
+            w.fused_moe(li.hidden, li.w13_q, li.w13_s, li.w13_z, li.w2_q, li.w2_s, li.w2_z, li.topk_ids,
+                        li.topk_w, wl.bits, wl.group_size, out=out, workspace=ws, events=events)
+        return li, ws, out, call
+
+    def timed(call, steps, warmup):
+        evs = new_events(steps)
+        run_steps(call, flush, warmup, None)
+        torch.cuda.synchronize()
+        run_steps(call, flush, steps, evs)
+        torch.cuda.synchronize()
+        per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(steps)])
+        return per  # ms: align, gather, gemm1, gemm2, combine
+
+    li, ws, out, call = setup(M)
+    # ---- the timed region
+    sampler = ClockSampler(local)
+    evs = new_events(args.steps)
+    run_steps(call, flush, args.warmup, None)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    run_steps(call, flush, args.steps, evs)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(args.steps)])
+    step_ms = per.sum(axis=1)
+    total_ms = float(step_ms.sum())
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * M * args.steps / (total_ms / 1000.0)
+
+    ids_np = li.topk_ids.cpu().numpy()
+    alg = algorithmic(wl, M, ids_np)
+    k1_ms, k2_ms = float(per[:, 2].mean()), float(per[:, 3].mean())
+    dom = ("gate_up_gemm", k1_ms, alg["gemm1_bytes"], alg["gemm1_flops"]) if k1_ms >= k2_ms else \
+        ("down_gemm", k2_ms, alg["gemm2_bytes"], alg["gemm2_flops"])
+    t_hbm = dom[2] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = dom[3] / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = dom[2] / (dom[1] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = dom[3] / (dom[1] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"]}
+    kname = f"moe_gemm_kernel<{wl.bits},{wl.act_dtype},{wl.scale_dtype},{1 if dom[0] == 'gate_up_gemm' else 2}>"
+    roof.update({"traffic": ncu_traffic(f"{wl.name}/M={M}", kname), "kernel": dom[0],
+                 "kernel_ms": dom[1], "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
+                 if peaks["source"] == "measured" else "fallback",
+                 "algorithmic_bytes": dom[2], "algorithmic_flops": dom[3]})
+
+    layer_s = ms_per_step / 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.act_dtype, "data": "synthetic",
+        "config": {
+            "workload": workload_label(wl, M), "M": M, "block": w.choose_block(M, wl.topk, wl.E),
+            "touched_experts": alg["touched"], "l2": "flushed before every step (512 MiB memset, outside the events)",
+            "parallelism": f"replicas x{world}",
+        },
+        "hbm": {"layer_algorithmic_bytes": alg["layer_bytes"], "layer_gbs": alg["layer_bytes"] / layer_s / 1e9,
+                "frac_of_peak": alg["layer_bytes"] / layer_s / 1e9 / peaks["hbm_gbs"],
+                "layer_tflops": alg["layer_flops"] / layer_s / 1e12},
+        "kernels_ms": {"align": float(per[:, 0].mean()), "gather": float(per[:, 1].mean()),
+                       "gate_up_gemm": k1_ms, "down_gemm": k2_ms, "combine": float(per[:, 4].mean())},
+        "roofline": roof,
+        "gpu_launches": 5 * args.steps * world,
+        "clocks": clocks,
+    }
+
+    if rank == 0 and not args.no_e2e:
+        line["e2e"] = e2e(w, wl, li, ws, flush, dev, max(10, min(args.steps, 100)))
+    if rank == 0 and not args.no_sweep:
+        sweep = []
+        for Mx in wl.m_sweep:
+            lix, _, _, callx = setup(Mx)
+            perx = timed(callx, args.sweep_steps, 3)
+            s = float(perx.sum(axis=1).mean()) / 1e3
+            a = algorithmic(wl, Mx, lix.topk_ids.cpu().numpy())
+            sweep.append({"M": Mx, "us": s * 1e6, "tokens_per_s": Mx / s, "hbm_gbs": a["layer_bytes"] / s / 1e9,
+                          "hbm_frac": a["layer_bytes"] / s / 1e9 / peaks["hbm_gbs"],
+                          "tflops": a["layer_flops"] / s / 1e12,
+                          "tensor_frac": a["layer_flops"] / s / 1e12 / peaks["bf16_tflops"],
+                          "touched_experts": a["touched"], "block": w.choose_block(Mx, wl.topk, wl.E),
+                          "kernels_us": [float(v) * 1e3 for v in perx.mean(axis=0)]})
+            del lix, callx
+        line["sweep"] = sweep
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, desc, secs = time_oracle(li, 10.0)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+                                "sample": desc + f" ({secs:.1f} s, numpy float64; BLAS may use all cores)"}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e(w, wl, li, ws, flush, dev, steps):
+    """Same metric through the public API with pinned host buffers: each step
+    copies the step's inputs host->device, runs the layer and reads the output
+    back; wall time per step, L2 flushed before each step outside the clock."""
+    M = li.hidden.shape[0]
+    h_x = li.hidden.cpu().pin_memory()
+    h_ids = li.topk_ids.cpu().pin_memory()
+    h_w = li.topk_w.cpu().pin_memory()
+    h_out = torch.empty(M, wl.H, dtype=li.hidden.dtype).pin_memory()
+    d_x, d_ids, d_w = torch.empty_like(li.hidden), torch.empty_like(li.topk_ids), torch.empty_like(li.topk_w)
+    d_out = torch.empty(M, wl.H, dtype=li.hidden.dtype, device=dev)
+    times = []
+    for i in range(steps + 3):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        d_x.copy_(h_x, non_blocking=True)
+        d_ids.copy_(h_ids, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        w.fused_moe(d_x, li.w13_q, li.w13_s, li.w13_z, li.w2_q, li.w2_s, li.w2_z, d_ids, d_w, wl.bits,
+                    wl.group_size, out=d_out, workspace=ws)
+        h_out.copy_(d_out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        if i >= 3:
+            times.append(time.perf_counter() - t0)
+    s = float(np.mean(times))
+    return {"value": M / s, "unit": "tokens/s", "ms_per_step": s * 1e3,
+            "h2d_bytes_per_step": h_x.numel() * h_x.element_size() + h_ids.numel() * 4 + h_w.numel() * 4,
+            "d2h_bytes_per_step": h_out.numel() * h_out.element_size()}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return ours_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -119,9 +119,10 @@ size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, i
                                        int bits, int group_size, int block, int split_k);
 
 /*
- * The fused layer: align -> gate/up GEMM with in-kernel dequant and
- * silu(gate)*up -> down GEMM with in-kernel dequant and the top-k weight ->
- * ordered top-k combine. One launch per stage (4 launches), none per expert.
+ * The fused layer: align -> gather of the routed token rows into expert order
+ * -> gate/up GEMM with in-kernel dequant and silu(gate)*up -> down GEMM with
+ * in-kernel dequant and the top-k weight -> ordered top-k combine. One launch
+ * per stage (5 launches), none per expert.
  *   hidden       [M, H] act_dtype.
  *   w13_q/w13_scales/w13_zeros, w2_q/w2_scales/w2_zeros: layout above
  *                (zeros may be NULL; both NULL or both non-NULL).
@@ -145,6 +146,23 @@ wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t 
                              int group_size, const int32_t* topk_ids,
                              const float* topk_weights, void* out, void* workspace,
                              size_t workspace_bytes, int block, int split_k, void* stream);
+
+/*
+ * wna16_fused_moe with per-launch timing: identical launches, and if
+ * `events` is non-NULL, events[i] (a cudaEvent_t, NULL entries skipped) is
+ * recorded on `stream` right before launch i (0 align, 1 token gather,
+ * 2 gate/up GEMM, 3 down GEMM, 4 combine) and events[5] after the last launch.
+ * For benchmarks.
+ */
+wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
+                                   int64_t I, int E, int topk, const int32_t* w13_q,
+                                   const void* w13_scales, const int32_t* w13_zeros,
+                                   const int32_t* w2_q, const void* w2_scales,
+                                   const int32_t* w2_zeros, wna16_dtype scale_dtype, int bits,
+                                   int group_size, const int32_t* topk_ids,
+                                   const float* topk_weights, void* out, void* workspace,
+                                   size_t workspace_bytes, int block, int split_k, void* stream,
+                                   void* const* events);
 
 /*
  * Synchronizes `stream`, then reads the device status word at the start of a

@@ -10,6 +10,7 @@ from .workloads import (  # noqa: F401
     WORKLOADS,
     Workload,
     LayerInputs,
+    make_expert_weights,
     make_layer_inputs,
     make_routing,
     make_hidden,

@@ -29,7 +29,8 @@ DEV_TIMEOUT = 0x2
 # Every symbol include/wna16_moe.h declares.
 EXPORTED = (
     "wna16_align_capacity", "wna16_moe_align_block_size", "wna16_choose_block",
-    "wna16_fused_moe_workspace_bytes", "wna16_fused_moe", "wna16_read_device_status",
+    "wna16_fused_moe_workspace_bytes", "wna16_fused_moe", "wna16_fused_moe_timed",
+    "wna16_read_device_status",
     "wna16_status_string",
 )
 
@@ -67,6 +68,8 @@ def load() -> ctypes.CDLL:
     L.wna16_fused_moe.argtypes = [vp, i32, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, i32, i32,
                                   i32, vp, vp, vp, vp, sz, i32, i32, vp]
     L.wna16_fused_moe.restype = i32
+    L.wna16_fused_moe_timed.argtypes = L.wna16_fused_moe.argtypes + [vp]
+    L.wna16_fused_moe_timed.restype = i32
     L.wna16_read_device_status.argtypes = [vp, c.POINTER(c.c_int32), vp]
     L.wna16_read_device_status.restype = i32
     L.wna16_status_string.argtypes = [i32]
@@ -153,8 +156,14 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
               w2_zeros: Optional[torch.Tensor], topk_ids: torch.Tensor, topk_weights: torch.Tensor,
               bits: int, group_size: int, out: Optional[torch.Tensor] = None,
               workspace: Optional[torch.Tensor] = None, block: int = 0, split_k: int = 0,
-              stream=None) -> torch.Tensor:
-    """The fused layer (see include/wna16_moe.h). Returns ``out`` [M, H]."""
+              stream=None, events=None) -> torch.Tensor:
+    """The fused layer (see include/wna16_moe.h). Returns ``out`` [M, H].
+
+    ``events``: optional list of 6 ``torch.cuda.Event`` (or None; each must
+    already exist on the device, i.e. have been recorded once) recorded before
+    the align, gather, gate/up GEMM, down GEMM and combine launches and after
+    the last.
+    """
     _check(hidden, "hidden", (torch.float16, torch.bfloat16))
     dev = hidden.device
     M, H = hidden.shape
@@ -183,11 +192,17 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     _check(workspace, "workspace", torch.uint8, device=dev)
-    st = load().wna16_fused_moe(
-        _ptr(hidden), _DTYPE[hidden.dtype], M, H, I, E, topk, _ptr(w13_q), _ptr(w13_scales),
-        _ptr(w13_zeros), _ptr(w2_q), _ptr(w2_scales), _ptr(w2_zeros), _DTYPE[w13_scales.dtype], bits,
-        group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out), _ptr(workspace),
-        workspace.numel(), block, split_k, _stream(stream))
+    args = (_ptr(hidden), _DTYPE[hidden.dtype], M, H, I, E, topk, _ptr(w13_q), _ptr(w13_scales),
+            _ptr(w13_zeros), _ptr(w2_q), _ptr(w2_scales), _ptr(w2_zeros), _DTYPE[w13_scales.dtype], bits,
+            group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out), _ptr(workspace),
+            workspace.numel(), block, split_k, _stream(stream))
+    if events is None:
+        st = load().wna16_fused_moe(*args)
+    else:
+        if len(events) != 6:
+            raise ValueError("events must hold 6 entries")
+        arr = (ctypes.c_void_p * 6)(*[None if e is None else e.cuda_event for e in events])
+        st = load().wna16_fused_moe_timed(*args, arr)
     _raise(st, "wna16_fused_moe")
     return out
 

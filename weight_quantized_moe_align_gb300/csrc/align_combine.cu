@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     moe_align_kernel(const int32_t* __restrict__ ids, int P, int E, int block, int cap,
                      int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
                      int32_t* __restrict__ num_post_pad, int32_t* __restrict__ counts_out,
-                     int32_t* __restrict__ status) {
+                     int32_t* __restrict__ status, int32_t* __restrict__ slot_of_pair) {
   __shared__ int cnt[kMaxExperts];
   __shared__ int off_end[kMaxExperts];      // exclusive end of each expert's padded segment
   __shared__ int run[kMaxExperts];          // next free slot of each expert
@@ -140,11 +140,33 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
       run[x] = r;
     }
     __syncthreads();
-    if (valid) sorted_ids[wbase[warp][e] + rank] = p;
+    if (valid) {
+      const int pos = wbase[warp][e] + rank;
+      sorted_ids[pos] = p;
+      if (slot_of_pair) slot_of_pair[p] = pos;
+    }
     __syncthreads();
     for (int x = tid; x < E; x += kAlignThreads)
       for (int w = 0; w < kAlignWarps; ++w) wbase[w][x] = 0;
     __syncthreads();
+  }
+}
+
+// Copies the hidden row of every routed pair to its expert-sorted slot:
+// x_sorted[slot_of_pair[p]] = hidden[p / topk] (16-byte vectors). Padded slots
+// are not written: they only feed MMA columns whose results are discarded.
+__global__ void __launch_bounds__(256)
+    moe_gather_kernel(const uint4* __restrict__ hidden, const int32_t* __restrict__ ids,
+                      const int32_t* __restrict__ slot_of_pair, int P, int topk, int E, int h8,
+                      uint4* __restrict__ x_sorted) {
+  const long long n = static_cast<long long>(P) * h8;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int p = static_cast<int>(idx / h8);
+    const int c = static_cast<int>(idx % h8);
+    const int e = ids[p];
+    if (e < 0 || e >= E) continue;
+    x_sorted[static_cast<long long>(slot_of_pair[p]) * h8 + c] = hidden[static_cast<long long>(p / topk) * h8 + c];
   }
 }
 
@@ -186,9 +208,22 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* num_post_pad, int32_t* counts,
-                         int32_t* status, cudaStream_t stream) {
+                         int32_t* status, int32_t* slot_of_pair, cudaStream_t stream) {
   moe_align_kernel<<<1, kAlignThreads, 0, stream>>>(ids, P, E, block, cap, sorted_ids, expert_ids,
-                                                    num_post_pad, counts, status);
+                                                    num_post_pad, counts, status, slot_of_pair);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
+                          int topk, int E, int H, int max_ctas, void* x_sorted, cudaStream_t stream) {
+  const int h8 = H / 8;
+  const long long n = static_cast<long long>(P) * h8;
+  const int threads = 256;
+  const long long want = (n + threads - 1) / threads;
+  const unsigned blocks = static_cast<unsigned>(want < max_ctas ? want : max_ctas);
+  if (blocks == 0) return cudaSuccess;
+  moe_gather_kernel<<<blocks, threads, 0, stream>>>(static_cast<const uint4*>(hidden), ids, slot_of_pair, P,
+                                                    topk, E, h8, static_cast<uint4*>(x_sorted));
   return cudaGetLastError();
 }
 

@@ -10,11 +10,10 @@ namespace wna16 {
 // Threads of the grouped-GEMM kernel and their roles (warp index):
 //   0      TMA producer (packed weights, scales, zero points)
 //   1      tcgen05 MMA issuer, owner of the TMEM allocation
-//   2..3   activation gatherers (cp.async rows of the token tile)
+//   2      token-tile loader (TMA; warp 3 idles)
 //   4..7   epilogue (TMEM -> registers -> global)
 //   8..15  dequantizers (shared -> registers -> TMEM A operand)
 constexpr int kGemmThreads = 512;
-constexpr int kLoaderThreads = 64;
 constexpr int kDequantWarps = 8;
 constexpr int kEpilogueWarps = 4;
 
@@ -23,10 +22,8 @@ constexpr int kTileRows = 128;   // weight rows per tile (MMA M)
 constexpr int kGateUpRows = 64;  // gate/up GEMM: 64 gate + 64 up rows per tile
 constexpr int kMaxStages = 24;
 constexpr int kMaxASlots = 8;
-constexpr int kLoaderLag = 4;    // cp.async groups in flight before signalling
 
 struct GemmArgs {
-  const uint8_t* b_src;        // token rows: hidden [M, K] or act cache [cap, K] (16-bit)
   const int32_t* sorted_ids;   // [cap]
   const int32_t* expert_ids;   // [cap / block]
   const int32_t* num_post_pad; // [1]
@@ -66,9 +63,9 @@ __host__ __device__ constexpr int weight_ring_bytes(int bits, int stages) {
 }
 __host__ __device__ constexpr int token_stage_bytes(int block) { return block * 128; }
 
-// Fixed extras after the two rings: per-thread loader row tables, barriers, flags.
-__host__ __device__ constexpr int gemm_extra_bytes(int block) {
-  return kLoaderThreads * (block / 8) * 4 + 8 * (3 * kMaxStages + 2 * kMaxASlots + 4 + 1) + 64;
+// Fixed extras after the two rings: barriers and flags.
+__host__ __device__ constexpr int gemm_extra_bytes(int /*block*/) {
+  return 8 * (3 * kMaxStages + 2 * kMaxASlots + 4 + 1) + 64;
 }
 __host__ __device__ constexpr int gemm_smem_bytes(int bits, int block, int stages) {
   return 1024 /* base alignment slack */ + weight_ring_bytes(bits, stages) +

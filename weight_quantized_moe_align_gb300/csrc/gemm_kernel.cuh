@@ -167,7 +167,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 template <int BITS, int ACT, int SCL, int GEMM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
-                    const __grid_constant__ CUtensorMap tm_z, const GemmArgs a) {
+                    const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_b,
+                    const GemmArgs a) {
   constexpr int PF = 32 / BITS;
   constexpr int KW = kTileK * BITS / 32;  // int32 words per row per stage
   constexpr int W_BYTES = kTileRows * KW * 4;
@@ -186,8 +187,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   uint8_t* wring = smem;
   uint8_t* bring = smem + weight_ring_bytes(BITS, NS);
-  int* rowtab = reinterpret_cast<int*>(bring + NS * BST);  // [NT/8][64]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rowtab + kLoaderThreads * (NT / 8));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bring + NS * BST);
   uint64_t* wfull = bars;
   uint64_t* bfull = wfull + NS;
   uint64_t* empty = bfull + NS;
@@ -202,11 +202,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&wfull[s], 1);
-      mbar_init(&bfull[s], kLoaderThreads);
+      mbar_init(&bfull[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < NA; ++i) {
-      mbar_init(&afull[i], kDequantWarps);
+      mbar_init(&afull[i], kDequantWarps / 2);  // one warpgroup per stage
       mbar_init(&aempty[i], 1);
     }
     for (int i = 0; i < NACC; ++i) {
@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_s);
+    prefetch_tmap(&tm_b);
     if (a.has_zeros) prefetch_tmap(&tm_z);
   }
   if (warp == 1) {
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   int nb = *a.num_post_pad / NT;
   nb = nb < 0 ? 0 : (nb > a.max_blocks ? a.max_blocks : nb);
   const int units = nb * a.n_tiles * a.split;
+  const uint64_t pol_b = l2_policy_evict_last();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -314,45 +316,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp < 4) {
-    // ------------------------------------------------------------ token gather
-    const int lt = threadIdx.x - 64;
-    const int nrow = NT / 8;  // rows handled by this thread: r = lt/8 + 8*i
-    int it = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const Unit w = decode_unit(u, nb, a);
-      for (int i = 0; i < nrow; ++i) {
-        const int r = (lt >> 3) + 8 * i;
-        const int slot = w.blk * NT + r;
-        const int pid = a.sorted_ids[slot];
-        int src = -1;
-        if (pid >= 0 && pid < a.P) src = (GEMM == 1) ? pid / a.topk : slot;
-        rowtab[i * kLoaderThreads + lt] = src;
-      }
-      const int c = lt & 7;
-      bool ok = true;
-      for (int kt = w.kt0; kt < w.kt1; ++kt) {
-        const int s = it % NS;
-        if (!wait_bar(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
-        const uint32_t dst = smem_u32(bring + s * BST);
-        for (int i = 0; i < nrow; ++i) {
-          const int r = (lt >> 3) + 8 * i;
-          const int src = rowtab[i * kLoaderThreads + lt];
-          const uint8_t* g = a.b_src + (static_cast<size_t>(src < 0 ? 0 : src) * a.K + kt * kTileK + c * 8) * 2;
-          cp_async_16(dst + r * 128 + ((c ^ (r & 7)) << 4), g, src >= 0 ? 16u : 0u);
+    // ------------------------------------------------------------ token tile (TMA)
+    // Warp 2 loads the B operand of every stage: the block's `block` rows of
+    // the expert-sorted token matrix (gathered hidden rows for gate/up, the act
+    // cache for down) as one TMA box in the 128-byte swizzled K-major layout
+    // the MMA descriptor describes.
+    if (warp == 2 && lane == 0) {
+      int it = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const Unit w = decode_unit(u, nb, a);
+        bool ok = true;
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
+          const int s = it % NS;
+          if (!wait_bar(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bfull[s], NT * 128);
+          tma_load_2d(bring + s * BST, &tm_b, &bfull[s], kt * kTileK, w.blk * NT, pol_b);
         }
-        cp_async_commit();
-        ++it;
-        if (it > kLoaderLag) {
-          cp_async_wait<kLoaderLag>();
-          fence_proxy_async_smem();
-          mbar_arrive(&bfull[(it - 1 - kLoaderLag) % NS]);
-        }
+        if (!ok) break;
       }
-      if (!ok) break;
+      for (int j = (it > NS ? it - NS : 0); j < it; ++j) wait_bar_drain(&bfull[j % NS], (j / NS) & 1);
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (int j = (it > kLoaderLag ? it - kLoaderLag : 0); j < it; ++j) mbar_arrive(&bfull[j % NS]);
   } else if (warp < 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
@@ -409,8 +392,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dequantizers
+    // Two warpgroups, stage-parallel: warpgroup g dequantizes the stages whose
+    // running index is congruent to g mod 2, one full 64-element K row per
+    // thread (thread = TMEM lane = weight row), so two stages are in flight.
     const int q = warp & 3;
-    const int half = (warp - 8) >> 2;  // which 32-element half of the stage's K
+    const int grp = (warp - 8) >> 2;
     int srow;
     if (GEMM == 1)
       srow = lane < 16 ? (16 * q + lane) : (kGateUpRows + 16 * q + lane - 16);
@@ -422,6 +408,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const Unit w = decode_unit(u, nb, a);
       bool ok = true;
       for (int kt = w.kt0; kt < w.kt1; ++kt, ++it, ++ait) {
+        if ((it & 1) != grp) continue;
         const int s = it % NS;
         const int slot = ait % NA;
         if (!warp_wait(&wfull[s], (it / NS) & 1, abort_flag, a.status) ||
@@ -438,19 +425,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint8_t* zbase = st + Z_OFF + ((GEMM == 1 && srow >= kGateUpRows) ? 128 : 0);
           zero = (reinterpret_cast<const uint32_t*>(zbase)[zr / PF] >> (BITS * (zr % PF))) & ZMASK;
         }
-        uint32_t wv[BITS];  // 32 K elements = BITS words
-        const uint4* src = reinterpret_cast<const uint4*>(st + srow * KW * 4 + half * BITS * 4);
+        const uint4* src = reinterpret_cast<const uint4*>(st + srow * KW * 4);
 #pragma unroll
-        for (int i = 0; i < BITS / 4; ++i) {
-          const uint4 x = src[i];
-          wv[4 * i + 0] = x.x;
-          wv[4 * i + 1] = x.y;
-          wv[4 * i + 2] = x.z;
-          wv[4 * i + 3] = x.w;
+        for (int h = 0; h < 2; ++h) {  // two 32-element halves of the row
+          uint32_t wv[BITS];
+#pragma unroll
+          for (int i = 0; i < BITS / 4; ++i) {
+            const uint4 x = src[h * (BITS / 4) + i];
+            wv[4 * i + 0] = x.x;
+            wv[4 * i + 1] = x.y;
+            wv[4 * i + 2] = x.z;
+            wv[4 * i + 3] = x.w;
+          }
+          uint32_t outv[16];
+          Dequant<BITS, ACT, SCL>::run(wv, zero, sbits, outv);
+          tmem_st16(tmem + t_lane + NACC * NT + slot * 32 + h * 16, outv);
         }
-        uint32_t outv[16];
-        Dequant<BITS, ACT, SCL>::run(wv, zero, sbits, outv);
-        tmem_st16(tmem + t_lane + NACC * NT + slot * 32 + half * 16, outv);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();

@@ -8,7 +8,7 @@ namespace {
 
 template <int ACT, int SCL, int GEMM>
 cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t stream, const CUtensorMap& q,
-                       const CUtensorMap& s, const CUtensorMap& z, const GemmArgs& a) {
+                       const CUtensorMap& s, const CUtensorMap& z, const CUtensorMap& b, const GemmArgs& a) {
   auto* fn = moe_gemm_kernel<8, ACT, SCL, GEMM>;
   // The opt-in shared-memory limit is per function and context; set it at most
   // once per device.
@@ -21,27 +21,27 @@ cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t stream, const CUtens
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  fn<<<grid, kGemmThreads, smem, stream>>>(q, s, z, a);
+  fn<<<grid, kGemmThreads, smem, stream>>>(q, s, z, b, a);
   return cudaGetLastError();
 }
 
 template <int GEMM>
 cudaError_t by_dtype(int act, int scl, dim3 grid, size_t smem, cudaStream_t stream,
                      const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
-                     const GemmArgs& a) {
-  if (act == 0 && scl == 0) return launch_one<0, 0, GEMM>(grid, smem, stream, q, s, z, a);
-  if (act == 0 && scl == 1) return launch_one<0, 1, GEMM>(grid, smem, stream, q, s, z, a);
-  if (act == 1 && scl == 0) return launch_one<1, 0, GEMM>(grid, smem, stream, q, s, z, a);
-  return launch_one<1, 1, GEMM>(grid, smem, stream, q, s, z, a);
+                     const CUtensorMap& b, const GemmArgs& a) {
+  if (act == 0 && scl == 0) return launch_one<0, 0, GEMM>(grid, smem, stream, q, s, z, b, a);
+  if (act == 0 && scl == 1) return launch_one<0, 1, GEMM>(grid, smem, stream, q, s, z, b, a);
+  if (act == 1 && scl == 0) return launch_one<1, 0, GEMM>(grid, smem, stream, q, s, z, b, a);
+  return launch_one<1, 1, GEMM>(grid, smem, stream, q, s, z, b, a);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_w8(int act, int scl, int gemm, dim3 grid, size_t smem,
                             cudaStream_t stream, const CUtensorMap& q, const CUtensorMap& s,
-                            const CUtensorMap& z, const GemmArgs& a) {
-  if (gemm == 1) return by_dtype<1>(act, scl, grid, smem, stream, q, s, z, a);
-  return by_dtype<2>(act, scl, grid, smem, stream, q, s, z, a);
+                            const CUtensorMap& z, const CUtensorMap& b, const GemmArgs& a) {
+  if (gemm == 1) return by_dtype<1>(act, scl, grid, smem, stream, q, s, z, b, a);
+  return by_dtype<2>(act, scl, grid, smem, stream, q, s, z, b, a);
 }
 
 }  // namespace wna16

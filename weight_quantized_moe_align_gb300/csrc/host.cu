@@ -8,7 +8,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/wna16_moe.h"
+#include "wna16_moe.h"
 #include "common.cuh"
 #include "gemm_launch.cuh"
 
@@ -79,7 +79,7 @@ int choose_split(int64_t units, int kt_total) {
 }
 
 struct WsLayout {
-  size_t status, sorted, experts, npp, counts, act, slab, total;
+  size_t status, sorted, experts, npp, counts, slot_of_pair, x_sorted, act, slab, total;
 };
 
 WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, int split) {
@@ -97,6 +97,8 @@ WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, 
   w.experts = take(static_cast<size_t>(cap / block) * 4);
   w.npp = take(4);
   w.counts = take(static_cast<size_t>(E) * 4);
+  w.slot_of_pair = take(static_cast<size_t>(P) * 4);
+  w.x_sorted = take(static_cast<size_t>(cap) * H * 2);
   w.act = take(static_cast<size_t>(cap) * I * 2);
   w.slab = take(static_cast<size_t>(split) * P * H * 4);
   w.total = o;
@@ -119,7 +121,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2D tiled map over a row-major [rows, cols] array, box {box_cols, box_rows}.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t cols,
-              uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+              uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
@@ -127,12 +130,12 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct GemmMaps {
-  CUtensorMap q, s, z;
+  CUtensorMap q, s, z, b;
 };
 
 // Maps of one projection: q [E*N, K/pf] int32, scales [E*K/G, N], zeros [E*K/G, N/pf].
@@ -151,8 +154,8 @@ bool make_gemm_maps(GemmMaps* g, const int32_t* q, const void* s, const int32_t*
 
 cudaError_t launch_gemm(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t st,
                         const GemmMaps& m, const GemmArgs& a) {
-  return bits == 4 ? launch_gemm_w4(act, scl, gemm, grid, smem, st, m.q, m.s, m.z, a)
-                   : launch_gemm_w8(act, scl, gemm, grid, smem, st, m.q, m.s, m.z, a);
+  return bits == 4 ? launch_gemm_w4(act, scl, gemm, grid, smem, st, m.q, m.s, m.z, m.b, a)
+                   : launch_gemm_w8(act, scl, gemm, grid, smem, st, m.q, m.s, m.z, m.b, a);
 }
 
 struct Resolved {
@@ -213,7 +216,7 @@ wna16_status wna16_moe_align_block_size(const int32_t* topk_ids, int64_t M, int 
     return WNA16_ERR_INVALID_ARG;
   const int64_t cap = capacity(P, E, block);
   if (launch_align(topk_ids, static_cast<int>(P), E, block, static_cast<int>(cap), sorted_ids, expert_ids,
-                   num_tokens_post_padded, expert_counts, device_status,
+                   num_tokens_post_padded, expert_counts, device_status, nullptr,
                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return WNA16_ERR_CUDA;
   return WNA16_OK;
@@ -226,13 +229,14 @@ size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, i
   return ws_layout(M, H, I, E, topk, r.block, r.split).total;
 }
 
-wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I,
-                             int E, int topk, const int32_t* w13_q, const void* w13_scales,
-                             const int32_t* w13_zeros, const int32_t* w2_q, const void* w2_scales,
-                             const int32_t* w2_zeros, wna16_dtype scale_dtype, int bits, int group_size,
-                             const int32_t* topk_ids, const float* topk_weights, void* out,
-                             void* workspace, size_t workspace_bytes, int block, int split_k,
-                             void* stream) {
+wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
+                                   int64_t I, int E, int topk, const int32_t* w13_q,
+                                   const void* w13_scales, const int32_t* w13_zeros, const int32_t* w2_q,
+                                   const void* w2_scales, const int32_t* w2_zeros,
+                                   wna16_dtype scale_dtype, int bits, int group_size,
+                                   const int32_t* topk_ids, const float* topk_weights, void* out,
+                                   void* workspace, size_t workspace_bytes, int block, int split_k,
+                                   void* stream, void* const* events) {
   if (act_dtype != WNA16_F16 && act_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
   if (scale_dtype != WNA16_F16 && scale_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
   Resolved r;
@@ -258,6 +262,8 @@ wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t 
   int32_t* experts = reinterpret_cast<int32_t*>(ws + L.experts);
   int32_t* npp = reinterpret_cast<int32_t*>(ws + L.npp);
   int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  int32_t* slot_of_pair = reinterpret_cast<int32_t*>(ws + L.slot_of_pair);
+  void* x_sorted = ws + L.x_sorted;
   void* act = ws + L.act;
   float* slab = reinterpret_cast<float*>(ws + L.slab);
 
@@ -267,21 +273,33 @@ wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t 
   const int max_blocks = static_cast<int>(cap / B);
   const bool zeros = w13_zeros != nullptr;
 
-  if (launch_align(topk_ids, P, E, B, static_cast<int>(cap), sorted, experts, npp, counts, status, s) !=
-      cudaSuccess)
-    return WNA16_ERR_CUDA;
-
+  auto mark = [&](int i) {
+    if (events && events[i]) return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+    return true;
+  };
   GemmMaps m1, m2;
   if (!make_gemm_maps(&m1, w13_q, w13_scales, zeros ? w13_zeros : nullptr, E, 2 * I, H, r.G1, bits,
                       kGateUpRows) ||
       !make_gemm_maps(&m2, w2_q, w2_scales, zeros ? w2_zeros : nullptr, E, H, I, r.G2, bits, kTileRows))
+    return WNA16_ERR_CUDA;
+  // Token tiles: `block` expert-sorted rows of 64 elements per stage, in the
+  // 128-byte swizzled K-major layout (gathered hidden rows; the act cache).
+  if (!make_map(&m1.b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, x_sorted, H, cap, kTileK, B,
+                CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m2.b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, act, I, cap, kTileK, B, CU_TENSOR_MAP_SWIZZLE_128B))
+    return WNA16_ERR_CUDA;
+
+  if (!mark(0) || launch_align(topk_ids, P, E, B, static_cast<int>(cap), sorted, experts, npp, counts, status,
+                               slot_of_pair, s) != cudaSuccess)
+    return WNA16_ERR_CUDA;
+  if (!mark(1) || launch_gather(hidden, topk_ids, slot_of_pair, P, topk, E, static_cast<int>(H), sm_count() * 8,
+                                x_sorted, s) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
   const Pipe pipe = pipe_for(bits, B);
   const int sms = sm_count();
 
   GemmArgs a1{};
-  a1.b_src = static_cast<const uint8_t*>(hidden);
   a1.sorted_ids = sorted;
   a1.expert_ids = experts;
   a1.num_post_pad = npp;
@@ -308,11 +326,10 @@ wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t 
   a1.tmem_cols = pipe.tmem_cols;
   const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles;
   const dim3 grid1(static_cast<unsigned>(std::min<int64_t>(units1, sms)));
-  if (launch_gemm(bits, act_dtype, scale_dtype, 1, grid1, pipe.smem, s, m1, a1) != cudaSuccess)
+  if (!mark(2) || launch_gemm(bits, act_dtype, scale_dtype, 1, grid1, pipe.smem, s, m1, a1) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
   GemmArgs a2 = a1;
-  a2.b_src = static_cast<const uint8_t*>(act);
   a2.out = slab;
   a2.K = static_cast<int>(I);
   a2.N = static_cast<int>(H);
@@ -324,13 +341,26 @@ wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t 
   a2.split = r.split;
   const int64_t units2 = static_cast<int64_t>(max_blocks) * a2.n_tiles * a2.split;
   const dim3 grid2(static_cast<unsigned>(std::min<int64_t>(units2, sms)));
-  if (launch_gemm(bits, act_dtype, scale_dtype, 2, grid2, pipe.smem, s, m2, a2) != cudaSuccess)
+  if (!mark(3) || launch_gemm(bits, act_dtype, scale_dtype, 2, grid2, pipe.smem, s, m2, a2) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
-  if (launch_combine(slab, topk_ids, static_cast<int>(M), static_cast<int>(H), topk, E, r.split,
-                     act_dtype, out, s) != cudaSuccess)
+  if (!mark(4) || launch_combine(slab, topk_ids, static_cast<int>(M), static_cast<int>(H), topk, E, r.split,
+                                 act_dtype, out, s) != cudaSuccess)
     return WNA16_ERR_CUDA;
+  if (!mark(5)) return WNA16_ERR_CUDA;
   return WNA16_OK;
+}
+
+wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I,
+                             int E, int topk, const int32_t* w13_q, const void* w13_scales,
+                             const int32_t* w13_zeros, const int32_t* w2_q, const void* w2_scales,
+                             const int32_t* w2_zeros, wna16_dtype scale_dtype, int bits, int group_size,
+                             const int32_t* topk_ids, const float* topk_weights, void* out,
+                             void* workspace, size_t workspace_bytes, int block, int split_k,
+                             void* stream) {
+  return wna16_fused_moe_timed(hidden, act_dtype, M, H, I, E, topk, w13_q, w13_scales, w13_zeros, w2_q,
+                               w2_scales, w2_zeros, scale_dtype, bits, group_size, topk_ids, topk_weights,
+                               out, workspace, workspace_bytes, block, split_k, stream, nullptr);
 }
 
 wna16_status wna16_read_device_status(const void* status_word, int32_t* bits_out, void* stream) {
