@@ -8,20 +8,24 @@
 namespace wna16 {
 
 // Threads of the grouped-GEMM kernel and their roles (warp index):
-//   0      TMA producer (packed weights, scales, zero points)
+//   0      TMA producer (packed weights, scales, zero points, token tile)
 //   1      tcgen05 MMA issuer, owner of the TMEM allocation
-//   2      token-tile loader (TMA; warp 3 idles)
-//   4..7   epilogue (TMEM -> registers -> global)
-//   8..15  dequantizers (shared -> registers -> TMEM A operand)
-constexpr int kGemmThreads = 512;
+//   2..5   epilogue (TMEM -> registers -> global); lane quarter = warp % 4
+//   6..13  dequantizers, two stage-parallel warpgroups (shared -> registers -> TMEM)
+// Token tiles up to 64 run two CTAs per SM (256 TMEM columns, <= 112 KB of
+// shared memory each) so two MMA streams overlap on the SM; larger tiles take
+// the whole SM.
+constexpr int kGemmThreads = 448;
 constexpr int kDequantWarps = 8;
 constexpr int kEpilogueWarps = 4;
 
-constexpr int kTileK = 64;       // K elements per pipeline stage
+constexpr int kTileK = 128;      // K elements per pipeline stage
+constexpr int kChunkK = 64;      // K elements per 128-byte swizzle atom of the token tile
 constexpr int kTileRows = 128;   // weight rows per tile (MMA M)
 constexpr int kGateUpRows = 64;  // gate/up GEMM: 64 gate + 64 up rows per tile
-constexpr int kMaxStages = 24;
+constexpr int kMaxStages = 16;
 constexpr int kMaxASlots = 8;
+constexpr int kASlotCols = kTileK / 2;  // TMEM columns of one stage's A operand (2 halves per column)
 
 struct GemmArgs {
   const int32_t* sorted_ids;   // [cap]
@@ -39,8 +43,8 @@ struct GemmArgs {
   int P;                       // M * topk
   int block;                   // align block = token tile (MMA N)
   int groups;                  // K / G
-  int kt_per_group;            // G / 64
-  int kt_total;                // K / 64
+  int G;                       // quantization group size along K (a multiple of 64)
+  int kt_total;                // ceil(K / 128) stages
   int split;                   // K splits (down GEMM), 1 otherwise
   int has_zeros;
   int max_blocks;              // cap / block
@@ -50,26 +54,22 @@ struct GemmArgs {
   uint32_t tmem_cols;
 };
 
-// Bytes of one weight stage in shared memory: packed codes of 128 rows x 64 K,
-// then 128 scales (256 B), then the zero-point words (two 128 B slots: the
-// gate/up GEMM loads gate and up zero points separately and every TMA
-// destination must be 128 B aligned). The token ring after the weight ring is 1 KB aligned
-// (128-byte-swizzle atoms).
-__host__ __device__ constexpr int weight_stage_bytes(int bits) {
-  return kTileRows * kTileK * bits / 8 + 256 + 256;
-}
+// One weight stage in shared memory: packed codes of 128 rows x 128 K, then up
+// to two group rows of 128 scales (512 B), then up to two group rows of zero
+// points (<= 256 B), each part 128-byte aligned (TMA destinations). The token
+// ring after the weight ring is 1 KB aligned (128-byte-swizzle atoms).
+__host__ __device__ constexpr int weight_code_bytes(int bits) { return kTileRows * kTileK * bits / 8; }
+__host__ __device__ constexpr int weight_stage_bytes(int bits) { return weight_code_bytes(bits) + 512 + 512; }
 __host__ __device__ constexpr int weight_ring_bytes(int bits, int stages) {
   return (stages * weight_stage_bytes(bits) + 1023) / 1024 * 1024;
 }
-__host__ __device__ constexpr int token_stage_bytes(int block) { return block * 128; }
+__host__ __device__ constexpr int token_stage_bytes(int block) { return (kTileK / kChunkK) * block * 128; }
 
 // Fixed extras after the two rings: barriers and flags.
-__host__ __device__ constexpr int gemm_extra_bytes(int /*block*/) {
-  return 8 * (3 * kMaxStages + 2 * kMaxASlots + 4 + 1) + 64;
-}
+__host__ __device__ constexpr int gemm_extra_bytes() { return 8 * (2 * kMaxStages + kMaxASlots + 4 + 1) + 64; }
 __host__ __device__ constexpr int gemm_smem_bytes(int bits, int block, int stages) {
-  return 1024 /* base alignment slack */ + weight_ring_bytes(bits, stages) +
-         stages * token_stage_bytes(block) + gemm_extra_bytes(block);
+  return 1024 /* base alignment slack */ + weight_ring_bytes(bits, stages) + stages * token_stage_bytes(block) +
+         gemm_extra_bytes();
 }
 
 }  // namespace wna16

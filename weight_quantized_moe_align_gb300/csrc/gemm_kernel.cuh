@@ -165,15 +165,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 template <int BITS, int ACT, int SCL, int GEMM>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, 2)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
                     const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_b,
                     const GemmArgs a) {
   constexpr int PF = 32 / BITS;
   constexpr int KW = kTileK * BITS / 32;  // int32 words per row per stage
-  constexpr int W_BYTES = kTileRows * KW * 4;
-  constexpr int S_OFF = W_BYTES;
-  constexpr int Z_OFF = W_BYTES + 256;
+  constexpr int W_BYTES = weight_code_bytes(BITS);
+  constexpr int S_OFF = W_BYTES;          // [SG][128] scales (gate/up: [SG][2 halves][64])
+  constexpr int Z_OFF = W_BYTES + 512;    // [SG][128 / PF] zero words (gate/up: [SG][2][64 / PF])
   constexpr int WST = weight_stage_bytes(BITS);
   constexpr uint32_t ZMASK = (1u << BITS) - 1;
 
@@ -184,16 +184,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int lane = threadIdx.x & 31;
   const int NS = a.num_stages, NA = a.num_aslots, NACC = a.num_acc, NT = a.block;
   const int BST = token_stage_bytes(NT);
+  const int SG = a.G < kTileK ? kTileK / a.G : 1;  // group rows per stage (G = 64 -> 2)
 
   uint8_t* wring = smem;
   uint8_t* bring = smem + weight_ring_bytes(BITS, NS);
   uint64_t* bars = reinterpret_cast<uint64_t*>(bring + NS * BST);
-  uint64_t* wfull = bars;
-  uint64_t* bfull = wfull + NS;
-  uint64_t* empty = bfull + NS;
-  uint64_t* afull = empty + NS;
-  uint64_t* aempty = afull + NA;
-  uint64_t* accfull = aempty + NA;
+  uint64_t* full = bars;             // stage landed: codes, scales, zeros and token tile
+  uint64_t* empty = full + NS;       // stage consumed: its MMAs completed (also frees its A slot)
+  uint64_t* afull = empty + NS;      // A slot written by a dequant warpgroup
+  uint64_t* accfull = afull + NA;    // accumulator ready for the epilogue
   uint64_t* accempty = accfull + NACC;
   uint64_t* drain = accempty + NACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -201,14 +200,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&wfull[s], 1);
-      mbar_init(&bfull[s], 1);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < NA; ++i) {
-      mbar_init(&afull[i], kDequantWarps / 2);  // one warpgroup per stage
-      mbar_init(&aempty[i], 1);
-    }
+    for (int i = 0; i < NA; ++i) mbar_init(&afull[i], kDequantWarps / 2);  // one warpgroup per stage
     for (int i = 0; i < NACC; ++i) {
       mbar_init(&accfull[i], 1);
       mbar_init(&accempty[i], kEpilogueWarps);
@@ -235,13 +230,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   int nb = *a.num_post_pad / NT;
   nb = nb < 0 ? 0 : (nb > a.max_blocks ? a.max_blocks : nb);
   const int units = nb * a.n_tiles * a.split;
-  const uint64_t pol_b = l2_policy_evict_last();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Per stage: codes of 128 rows (gate/up: one 3D box holding the 64 gate and
+    // the 64 up rows), their scales and zero points (one box each), and the two
+    // 64-wide K chunks of the token tile: five copies for 8-16 KB of codes.
     if (lane == 0) {
-      const uint32_t stage_tx = W_BYTES + 256 + (a.has_zeros ? (kTileRows / PF) * 4 : 0);
-      const uint64_t pol = l2_policy_evict_first();
+      const uint32_t stage_tx = W_BYTES + SG * 256 + (a.has_zeros ? SG * (kTileRows / PF) * 4 : 0) + BST;
+      const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+      const uint64_t pol_b = l2_policy_evict_last();   // token rows: re-read by every row tile
       int it = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const Unit w = decode_unit(u, nb, a);
@@ -250,36 +248,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
           const int s = it % NS;
           if (!wait_bar(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&wfull[s], stage_tx);
+          mbar_arrive_expect_tx(&full[s], stage_tx);
           uint8_t* dst = wring + s * WST;
-          const int ys = e * a.groups + kt / a.kt_per_group;
+          const int ys = e * a.groups + (kt * kTileK) / a.G;
           if (GEMM == 1) {
             const int f0 = w.tile * kGateUpRows;
-            tma_load_2d(dst, &tm_q, &wfull[s], kt * KW, e * a.N + f0, pol);
-            tma_load_2d(dst + kGateUpRows * KW * 4, &tm_q, &wfull[s], kt * KW, e * a.N + a.I + f0, pol);
-            tma_load_2d(dst + S_OFF, &tm_s, &wfull[s], f0, ys, pol);
-            tma_load_2d(dst + S_OFF + 128, &tm_s, &wfull[s], a.I + f0, ys, pol);
-            if (a.has_zeros) {
-              tma_load_2d(dst + Z_OFF, &tm_z, &wfull[s], f0 / PF, ys, pol);
-              tma_load_2d(dst + Z_OFF + 128, &tm_z, &wfull[s], (a.I + f0) / PF, ys, pol);
-            }
+            tma_load_3d(dst, &tm_q, &full[s], kt * KW, f0, 2 * e, pol_w);
+            tma_load_3d(dst + S_OFF, &tm_s, &full[s], f0, 0, ys, pol_w);
+            if (a.has_zeros) tma_load_3d(dst + Z_OFF, &tm_z, &full[s], f0 / PF, 0, ys, pol_w);
           } else {
             const int r0 = w.tile * kTileRows;
-            tma_load_2d(dst, &tm_q, &wfull[s], kt * KW, e * a.N + r0, pol);
-            tma_load_2d(dst + S_OFF, &tm_s, &wfull[s], r0, ys, pol);
-            if (a.has_zeros) tma_load_2d(dst + Z_OFF, &tm_z, &wfull[s], r0 / PF, ys, pol);
+            tma_load_2d(dst, &tm_q, &full[s], kt * KW, e * a.N + r0, pol_w);
+            tma_load_2d(dst + S_OFF, &tm_s, &full[s], r0, ys, pol_w);
+            if (a.has_zeros) tma_load_2d(dst + Z_OFF, &tm_z, &full[s], r0 / PF, ys, pol_w);
           }
+          // token tile: the block's rows of the expert-sorted token matrix
+#pragma unroll
+          for (int c = 0; c < kTileK / kChunkK; ++c)
+            tma_load_2d(bring + s * BST + c * NT * 128, &tm_b, &full[s], kt * kTileK + c * kChunkK, w.blk * NT,
+                        pol_b);
         }
         if (!ok) break;
       }
       // Let every issued copy land before the CTA can exit.
-      for (int j = (it > NS ? it - NS : 0); j < it; ++j) wait_bar_drain(&wfull[j % NS], (j / NS) & 1);
+      for (int j = (it > NS ? it - NS : 0); j < it; ++j) wait_bar_drain(&full[j % NS], (j / NS) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(ACT, NT);
-      int it = 0, ait = 0, uc = 0;
+      int it = 0, uc = 0;
       bool issued = false;
       for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
         const Unit w = decode_unit(u, nb, a);
@@ -288,23 +286,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * NT;
         bool ok = true;
-        for (int kt = w.kt0; kt < w.kt1; ++kt, ++it, ++ait) {
+        for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
           const int s = it % NS;
-          const int slot = ait % NA;
-          if (!wait_bar(&afull[slot], (ait / NA) & 1, abort_flag, a.status) ||
-              !wait_bar(&bfull[s], (it / NS) & 1, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
+          const int slot = it % NA;
+          // afull implies the stage landed (the dequant warps waited on full[s])
+          if (!wait_bar(&afull[slot], (it / NA) & 1, abort_flag, a.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_tmem = tmem + NACC * NT + slot * 32;
-          const uint32_t b_addr = smem_u32(bring + s * BST);
+          const uint32_t a_tmem = tmem + NACC * NT + slot * kASlotCols;
+          const uint64_t b_desc = smem_desc_sw128(smem_u32(bring + s * BST));
+          const uint64_t chunk_step = static_cast<uint64_t>((NT * 128) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk)
-            mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
-                   (kt > w.kt0 || kk > 0) ? 1u : 0u);
+            mma_ts(d_tmem, a_tmem + kk * 8, b_desc + (kk / 4) * chunk_step + 2 * (kk % 4) /* 32 B per K=16 */,
+                   idesc, (kt > w.kt0 || kk > 0) ? 1u : 0u);
           mma_commit(&empty[s]);
-          mma_commit(&aempty[slot]);
           issued = true;
         }
         if (!ok) break;
@@ -315,30 +310,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         wait_bar_drain(drain, 0);
       }
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ token tile (TMA)
-    // Warp 2 loads the B operand of every stage: the block's `block` rows of
-    // the expert-sorted token matrix (gathered hidden rows for gate/up, the act
-    // cache for down) as one TMA box in the 128-byte swizzled K-major layout
-    // the MMA descriptor describes.
-    if (warp == 2 && lane == 0) {
-      int it = 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const Unit w = decode_unit(u, nb, a);
-        bool ok = true;
-        for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
-          const int s = it % NS;
-          if (!wait_bar(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bfull[s], NT * 128);
-          tma_load_2d(bring + s * BST, &tm_b, &bfull[s], kt * kTileK, w.blk * NT, pol_b);
-        }
-        if (!ok) break;
-      }
-      for (int j = (it > NS ? it - NS : 0); j < it; ++j) wait_bar_drain(&bfull[j % NS], (j / NS) & 1);
-    }
-  } else if (warp < 8) {
+  } else if (warp < 2 + kEpilogueWarps) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
     int uc = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
       const Unit w = decode_unit(u, nb, a);
@@ -393,41 +367,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------ dequantizers
     // Two warpgroups, stage-parallel: warpgroup g dequantizes the stages whose
-    // running index is congruent to g mod 2, one full 64-element K row per
+    // running index is congruent to g mod 2, one full 128-element K row per
     // thread (thread = TMEM lane = weight row), so two stages are in flight.
+    // A slot it % NA is free once the MMAs of stage it - NA completed, which is
+    // the completion of that stage's `empty` phase.
     const int q = warp & 3;
-    const int grp = (warp - 8) >> 2;
-    int srow;
-    if (GEMM == 1)
-      srow = lane < 16 ? (16 * q + lane) : (kGateUpRows + 16 * q + lane - 16);
-    else
+    const int grp = (warp - 2 - kEpilogueWarps) >> 2;
+    // Weight row (in the stage's smem tile) of this thread's TMEM lane. Gate/up:
+    // lanes 0-15 of quarter q take gate rows 16q.., lanes 16-31 the up rows of
+    // the same features, so the epilogue finds gate and up in one warp.
+    int srow, half = 0, hrow;
+    if (GEMM == 1) {
+      half = lane < 16 ? 0 : 1;
+      hrow = 16 * q + (lane & 15);
+      srow = half * kGateUpRows + hrow;
+    } else {
       srow = q * 32 + lane;
+      hrow = srow;
+    }
     const uint32_t t_lane = (q * 32) << 16;
-    int it = 0, ait = 0;
+    int it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = decode_unit(u, nb, a);
       bool ok = true;
-      for (int kt = w.kt0; kt < w.kt1; ++kt, ++it, ++ait) {
+      for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
         if ((it & 1) != grp) continue;
         const int s = it % NS;
-        const int slot = ait % NA;
-        if (!warp_wait(&wfull[s], (it / NS) & 1, abort_flag, a.status) ||
-            !warp_wait(&aempty[slot], ((ait / NA) & 1) ^ 1, abort_flag, a.status)) {
-          ok = false;
-          break;
+        const int slot = it % NA;
+        if (!warp_wait(&full[s], (it / NS) & 1, abort_flag, a.status)) { ok = false; break; }
+        if (it >= NA) {
+          const int prev = it - NA;
+          if (!warp_wait(&empty[prev % NS], (prev / NS) & 1, abort_flag, a.status)) { ok = false; break; }
         }
         const uint8_t* st = wring + s * WST;
-        const uint32_t sbits = reinterpret_cast<const uint16_t*>(st + S_OFF)[srow];
-        uint32_t zero = 1u << (BITS - 1);
-        if (a.has_zeros) {
-          // gate/up: rows [64, 128) are the up rows, their zero words start at +128 B
-          const int zr = (GEMM == 1 && srow >= kGateUpRows) ? srow - kGateUpRows : srow;
-          const uint8_t* zbase = st + Z_OFF + ((GEMM == 1 && srow >= kGateUpRows) ? 128 : 0);
-          zero = (reinterpret_cast<const uint32_t*>(zbase)[zr / PF] >> (BITS * (zr % PF))) & ZMASK;
+        // scale and zero point of each 64-wide chunk of the stage (group rows 0/1 when G = 64)
+        uint32_t sbits[2], zero[2];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int gr = SG == 2 ? c : 0;
+          const int si = GEMM == 1 ? (gr * 2 + half) * kGateUpRows + hrow : gr * kTileRows + hrow;
+          sbits[c] = reinterpret_cast<const uint16_t*>(st + S_OFF)[si];
+          zero[c] = 1u << (BITS - 1);
+          if (a.has_zeros) {
+            const int zi = GEMM == 1 ? (gr * 2 + half) * (kGateUpRows / PF) + hrow / PF
+                                     : gr * (kTileRows / PF) + hrow / PF;
+            zero[c] = (reinterpret_cast<const uint32_t*>(st + Z_OFF)[zi] >> (BITS * (hrow % PF))) & ZMASK;
+          }
         }
         const uint4* src = reinterpret_cast<const uint4*>(st + srow * KW * 4);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {  // two 32-element halves of the row
+        for (int h = 0; h < 4; ++h) {  // four 32-element quarters of the row
           uint32_t wv[BITS];
 #pragma unroll
           for (int i = 0; i < BITS / 4; ++i) {
@@ -438,8 +427,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             wv[4 * i + 3] = x.w;
           }
           uint32_t outv[16];
-          Dequant<BITS, ACT, SCL>::run(wv, zero, sbits, outv);
-          tmem_st16(tmem + t_lane + NACC * NT + slot * 32 + h * 16, outv);
+          Dequant<BITS, ACT, SCL>::run(wv, zero[h >> 1], sbits[h >> 1], outv);
+          tmem_st16(tmem + t_lane + NACC * NT + slot * kASlotCols + h * 16, outv);
         }
         tmem_st_wait();
         tc_fence_before();

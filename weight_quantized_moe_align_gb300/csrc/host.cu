@@ -16,8 +16,9 @@ using namespace wna16;
 
 namespace {
 
-constexpr int kMaxSmem = 232448;  // opt-in dynamic shared memory per CTA on sm_103a
-constexpr int kMinSmem = 120 * 1024;  // keeps one GEMM CTA per SM (TMEM is not shared)
+constexpr int kMaxSmem = 232448;   // opt-in dynamic shared memory per CTA on sm_103a
+constexpr int kHalfSmem = 112 * 1024;  // two CTAs per SM
+constexpr int kMinSmem = 120 * 1024;   // a whole-SM CTA (512 TMEM columns) runs alone on its SM
 
 bool is_pow2(long long v) { return v > 0 && (v & (v - 1)) == 0; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -49,30 +50,34 @@ int choose_block_impl(int64_t M, int topk, int E) {
   return b;
 }
 
-// Pipeline shape of one GEMM launch for a token tile of `block`.
+// Pipeline shape of one GEMM launch for a token tile of `block`. Token tiles up
+// to 64 use half of the SM (256 TMEM columns, <= 112 KB of shared memory) so two
+// CTAs, and so two MMA streams, share each SM; larger tiles take the whole SM.
 struct Pipe {
-  int stages, aslots, acc;
+  int stages, aslots, acc, ctas_per_sm;
   uint32_t tmem_cols;
   size_t smem;
 };
 
 Pipe pipe_for(int bits, int block) {
   Pipe p;
-  p.acc = block <= 128 ? 2 : 1;
-  p.aslots = std::min(kMaxASlots, (512 - p.acc * block) / 32);
-  const int need = p.acc * block + p.aslots * 32;
-  p.tmem_cols = 32;
-  while (static_cast<int>(p.tmem_cols) < need) p.tmem_cols <<= 1;
+  const bool half_sm = block <= 64;
+  p.ctas_per_sm = half_sm ? 2 : 1;
+  p.tmem_cols = half_sm ? 256 : 512;
+  const int smem_cap = half_sm ? kHalfSmem : kMaxSmem;
+  p.acc = (2 * block + 2 * kASlotCols <= static_cast<int>(p.tmem_cols)) ? 2 : 1;
   p.stages = kMaxStages;
-  while (p.stages > 2 && gemm_smem_bytes(bits, block, p.stages) > kMaxSmem) --p.stages;
-  p.smem = std::max<size_t>(gemm_smem_bytes(bits, block, p.stages), kMinSmem);
+  while (p.stages > 2 && gemm_smem_bytes(bits, block, p.stages) > smem_cap) --p.stages;
+  p.aslots = std::min({kMaxASlots, (static_cast<int>(p.tmem_cols) - p.acc * block) / kASlotCols, p.stages - 1});
+  p.smem = gemm_smem_bytes(bits, block, p.stages);
+  if (!half_sm) p.smem = std::max<size_t>(p.smem, kMinSmem);
   return p;
 }
 
-int choose_split(int64_t units, int kt_total) {
-  const int sms = sm_count();
-  if (units >= sms) return 1;
-  int s = static_cast<int>(sms / std::max<int64_t>(units, 1));
+int choose_split(int64_t units, int kt_total, int ctas_per_sm) {
+  const int slots = sm_count() * ctas_per_sm;
+  if (units >= slots) return 1;
+  int s = static_cast<int>(slots / std::max<int64_t>(units, 1));
   s = std::min(s, 8);
   s = std::min(s, std::max(1, kt_total / 8));  // keep >= 8 K stages per split
   return std::max(s, 1);
@@ -119,37 +124,83 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D tiled map over a row-major [rows, cols] array, box {box_cols, box_rows}.
-bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t cols,
-              uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+// Tiled map of rank 2 or 3: dims[0] innermost (elements), strides in bytes of
+// dims 1.. (dims[0] is contiguous).
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box,
               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * elem_bytes};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  cuuint64_t d[3], st[2];
+  cuuint32_t b[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+  return fn(m, dt, rank, const_cast<void*>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct GemmMaps {
   CUtensorMap q, s, z, b;
 };
 
-// Maps of one projection: q [E*N, K/pf] int32, scales [E*K/G, N], zeros [E*K/G, N/pf].
+// Maps of one projection, one box per stage each:
+//   gate/up (rows = 2I): codes [E*2 halves, I, K/pf] box {128/pf, 64, 2} (gate rows
+//   then the matching up rows), scales [E*K/G, 2, I] box {64, 2, SG}, zeros
+//   [E*K/G, 2, I/pf] box {64/pf, 2, SG};
+//   down (rows = H): codes [E*H, K/pf] box {128/pf, 128}, scales [E*K/G, H] box
+//   {128, SG}, zeros [E*K/G, H/pf] box {128/pf, SG}.
 bool make_gemm_maps(GemmMaps* g, const int32_t* q, const void* s, const int32_t* z, int E, int64_t N,
-                    int64_t K, int G, int bits, uint32_t box_rows) {
+                    int64_t K, int G, int bits, bool gate_up) {
   const int pf = 32 / bits;
-  const int64_t groups = K / G;
+  const uint64_t groups = K / G;
+  const uint32_t sg = G < kTileK ? kTileK / G : 1;
+  const uint32_t kw = kTileK / pf;
   std::memset(g, 0, sizeof(*g));
-  if (!make_map(&g->q, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, q, K / pf, E * N, kTileK / pf, box_rows))
-    return false;
-  if (!make_map(&g->s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, s, N, E * groups, box_rows, 1)) return false;
-  if (z && !make_map(&g->z, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, z, N / pf, E * groups, box_rows / pf, 1))
-    return false;
+  if (gate_up) {
+    const uint64_t I = N / 2;
+    const uint64_t qd[3] = {static_cast<uint64_t>(K / pf), I, 2ull * E};
+    const uint64_t qs[2] = {static_cast<uint64_t>(K / pf) * 4, I * (K / pf) * 4};
+    const uint32_t qb[3] = {kw, kGateUpRows, 2};
+    if (!make_map(&g->q, CU_TENSOR_MAP_DATA_TYPE_INT32, q, 3, qd, qs, qb)) return false;
+    const uint64_t sd[3] = {I, 2, E * groups};
+    const uint64_t ss[2] = {I * 2, 2 * I * 2};
+    const uint32_t sb[3] = {kGateUpRows, 2, sg};
+    if (!make_map(&g->s, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, 3, sd, ss, sb)) return false;
+    if (z) {
+      const uint64_t zd[3] = {I / pf, 2, E * groups};
+      const uint64_t zs[2] = {(I / pf) * 4, 2 * (I / pf) * 4};
+      const uint32_t zb[3] = {static_cast<uint32_t>(kGateUpRows / pf), 2, sg};
+      if (!make_map(&g->z, CU_TENSOR_MAP_DATA_TYPE_INT32, z, 3, zd, zs, zb)) return false;
+    }
+  } else {
+    const uint64_t qd[2] = {static_cast<uint64_t>(K / pf), static_cast<uint64_t>(E) * N};
+    const uint64_t qs[1] = {static_cast<uint64_t>(K / pf) * 4};
+    const uint32_t qb[2] = {kw, kTileRows};
+    if (!make_map(&g->q, CU_TENSOR_MAP_DATA_TYPE_INT32, q, 2, qd, qs, qb)) return false;
+    const uint64_t sd[2] = {static_cast<uint64_t>(N), E * groups};
+    const uint64_t ss[1] = {static_cast<uint64_t>(N) * 2};
+    const uint32_t sb[2] = {kTileRows, sg};
+    if (!make_map(&g->s, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, 2, sd, ss, sb)) return false;
+    if (z) {
+      const uint64_t zd[2] = {static_cast<uint64_t>(N / pf), E * groups};
+      const uint64_t zs[1] = {static_cast<uint64_t>(N / pf) * 4};
+      const uint32_t zb[2] = {static_cast<uint32_t>(kTileRows / pf), sg};
+      if (!make_map(&g->z, CU_TENSOR_MAP_DATA_TYPE_INT32, z, 2, zd, zs, zb)) return false;
+    }
+  }
   return true;
+}
+
+// Token tile map: rows of a [rows, K] 16-bit matrix, box {64, block} in the
+// 128-byte swizzled layout (two boxes per 128-wide stage).
+bool make_token_map(CUtensorMap* m, const void* base, int64_t K, int64_t rows, int block) {
+  const uint64_t d[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows)};
+  const uint64_t st[1] = {static_cast<uint64_t>(K) * 2};
+  const uint32_t b[2] = {kChunkK, static_cast<uint32_t>(block)};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, base, 2, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 cudaError_t launch_gemm(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t st,
@@ -174,19 +225,22 @@ wna16_status resolve(int64_t M, int64_t H, int64_t I, int E, int topk, int bits,
     r->G1 = static_cast<int>(H);
     r->G2 = static_cast<int>(I);
   } else {
+    // A 128-wide K stage must not straddle two groups: G = 64 (two groups per
+    // stage) or a multiple of 128.
     if (group_size <= 0) return WNA16_ERR_INVALID_ARG;
-    if (group_size % 64 || H % group_size || I % group_size) return WNA16_ERR_UNSUPPORTED;
+    if ((group_size != 64 && group_size % kTileK) || H % group_size || I % group_size)
+      return WNA16_ERR_UNSUPPORTED;
     r->G1 = r->G2 = group_size;
   }
   if (block == 0) block = choose_block_impl(M, topk, E);
   if (!is_pow2(block) || block < 16 || block > 256) return WNA16_ERR_INVALID_ARG;
   r->block = block;
   if (split_k < 0 || split_k > 8) return WNA16_ERR_INVALID_ARG;
-  const int kt2 = static_cast<int>(I / kTileK);
+  const int kt2 = static_cast<int>((I + kTileK - 1) / kTileK);
   if (split_k == 0) {
     const int64_t blocks = capacity(M * topk, E, block) / block;
     const int64_t units = blocks * ((H + kTileRows - 1) / kTileRows);
-    split_k = choose_split(units, kt2);
+    split_k = choose_split(units, kt2, pipe_for(bits, block).ctas_per_sm);
   }
   r->split = std::min(split_k, kt2);
   return WNA16_OK;
@@ -278,15 +332,12 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
     return true;
   };
   GemmMaps m1, m2;
-  if (!make_gemm_maps(&m1, w13_q, w13_scales, zeros ? w13_zeros : nullptr, E, 2 * I, H, r.G1, bits,
-                      kGateUpRows) ||
-      !make_gemm_maps(&m2, w2_q, w2_scales, zeros ? w2_zeros : nullptr, E, H, I, r.G2, bits, kTileRows))
+  if (!make_gemm_maps(&m1, w13_q, w13_scales, zeros ? w13_zeros : nullptr, E, 2 * I, H, r.G1, bits, true) ||
+      !make_gemm_maps(&m2, w2_q, w2_scales, zeros ? w2_zeros : nullptr, E, H, I, r.G2, bits, false))
     return WNA16_ERR_CUDA;
   // Token tiles: `block` expert-sorted rows of 64 elements per stage, in the
   // 128-byte swizzled K-major layout (gathered hidden rows; the act cache).
-  if (!make_map(&m1.b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, x_sorted, H, cap, kTileK, B,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&m2.b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, act, I, cap, kTileK, B, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!make_token_map(&m1.b, x_sorted, H, cap, B) || !make_token_map(&m2.b, act, I, cap, B))
     return WNA16_ERR_CUDA;
 
   if (!mark(0) || launch_align(topk_ids, P, E, B, static_cast<int>(cap), sorted, experts, npp, counts, status,
@@ -315,8 +366,8 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a1.P = P;
   a1.block = B;
   a1.groups = static_cast<int>(H / r.G1);
-  a1.kt_per_group = r.G1 / kTileK;
-  a1.kt_total = static_cast<int>(H / kTileK);
+  a1.G = r.G1;
+  a1.kt_total = static_cast<int>((H + kTileK - 1) / kTileK);
   a1.split = 1;
   a1.has_zeros = zeros ? 1 : 0;
   a1.max_blocks = max_blocks;
@@ -325,7 +376,8 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a1.num_acc = pipe.acc;
   a1.tmem_cols = pipe.tmem_cols;
   const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles;
-  const dim3 grid1(static_cast<unsigned>(std::min<int64_t>(units1, sms)));
+  const int64_t slots = static_cast<int64_t>(sms) * pipe.ctas_per_sm;
+  const dim3 grid1(static_cast<unsigned>(std::min<int64_t>(units1, slots)));
   if (!mark(2) || launch_gemm(bits, act_dtype, scale_dtype, 1, grid1, pipe.smem, s, m1, a1) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
@@ -336,11 +388,11 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a2.I = 0;
   a2.n_tiles = static_cast<int>((H + kTileRows - 1) / kTileRows);
   a2.groups = static_cast<int>(I / r.G2);
-  a2.kt_per_group = r.G2 / kTileK;
-  a2.kt_total = static_cast<int>(I / kTileK);
+  a2.G = r.G2;
+  a2.kt_total = static_cast<int>((I + kTileK - 1) / kTileK);
   a2.split = r.split;
   const int64_t units2 = static_cast<int64_t>(max_blocks) * a2.n_tiles * a2.split;
-  const dim3 grid2(static_cast<unsigned>(std::min<int64_t>(units2, sms)));
+  const dim3 grid2(static_cast<unsigned>(std::min<int64_t>(units2, slots)));
   if (!mark(3) || launch_gemm(bits, act_dtype, scale_dtype, 2, grid2, pipe.smem, s, m2, a2) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
