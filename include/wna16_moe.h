@@ -165,6 +165,48 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
                                    void* const* events);
 
 /*
+ * Size of the library-owned scratch area used by wna16_fused_moe_noalloc:
+ * 64 MiB, reserved on every GPU that loads the library, for as long as the
+ * library stays loaded.
+ */
+#define WNA16_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * wna16_fused_moe for callers that cannot hand the library a workspace. The
+ * pages this library follows have no counterpart of this entry point; it exists
+ * for host code that has no allocator to draw from: a plain C program or a
+ * plugin living inside a process whose memory manager owns the device memory
+ * (where an extra cudaMalloc would fail against a fixed budget or break that
+ * manager's bookkeeping). It takes the same arguments as wna16_fused_moe minus
+ * the workspace, and allocates nothing: the workspace is a fixed area of
+ * WNA16_NOALLOC_SCRATCH_BYTES inside the library's own device data.
+ *   - Sizes whose wna16_fused_moe_workspace_bytes() exceeds
+ *     WNA16_NOALLOC_SCRATCH_BYTES are rejected with
+ *     WNA16_ERR_WORKSPACE_TOO_SMALL before anything is launched (decode-sized
+ *     batches of the supported layers fit; large prefill batches do not: use
+ *     wna16_fused_moe with a workspace for those).
+ *   - The first call on a device looks up the area's device address on the
+ *     current device (a one-time set-up per device); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one area, which keeps whatever the
+ *     last call left in it. Each call rewrites everything it later reads (the
+ *     device status word at its start is reset by the call), so nothing has
+ *     to be cleared between calls; that status word is not reachable from
+ *     outside the library.
+ *   - Calls whose GPU execution overlaps (issued on different streams, or
+ *     from different host threads without ordering) race on the area and
+ *     corrupt each other's results: serialize them.
+ */
+wna16_status wna16_fused_moe_noalloc(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
+                                     int64_t I, int E, int topk, const int32_t* w13_q,
+                                     const void* w13_scales, const int32_t* w13_zeros,
+                                     const int32_t* w2_q, const void* w2_scales,
+                                     const int32_t* w2_zeros, wna16_dtype scale_dtype, int bits,
+                                     int group_size, const int32_t* topk_ids,
+                                     const float* topk_weights, void* out, int block, int split_k,
+                                     void* stream);
+
+/*
  * Synchronizes `stream`, then reads the device status word at the start of a
  * fused-call workspace (or any int32 status word the caller passed to the
  * align call). Writes the raw bits to *bits_out (may be NULL) and returns

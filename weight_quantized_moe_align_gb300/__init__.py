@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     align_capacity,
     choose_block,
     fused_moe,
+    fused_moe_noalloc,
     load,
     moe_align_block_size,
     read_device_status,

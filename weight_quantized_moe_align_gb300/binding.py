@@ -30,7 +30,7 @@ DEV_TIMEOUT = 0x2
 EXPORTED = (
     "wna16_align_capacity", "wna16_moe_align_block_size", "wna16_choose_block",
     "wna16_fused_moe_workspace_bytes", "wna16_fused_moe", "wna16_fused_moe_timed",
-    "wna16_read_device_status",
+    "wna16_fused_moe_noalloc", "wna16_read_device_status",
     "wna16_status_string",
 )
 
@@ -70,6 +70,8 @@ def load() -> ctypes.CDLL:
     L.wna16_fused_moe.restype = i32
     L.wna16_fused_moe_timed.argtypes = L.wna16_fused_moe.argtypes + [vp]
     L.wna16_fused_moe_timed.restype = i32
+    L.wna16_fused_moe_noalloc.argtypes = L.wna16_fused_moe.argtypes[:19] + [i32, i32, vp]
+    L.wna16_fused_moe_noalloc.restype = i32
     L.wna16_read_device_status.argtypes = [vp, c.POINTER(c.c_int32), vp]
     L.wna16_read_device_status.restype = i32
     L.wna16_status_string.argtypes = [i32]
@@ -204,6 +206,34 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
         arr = (ctypes.c_void_p * 6)(*[None if e is None else e.cuda_event for e in events])
         st = load().wna16_fused_moe_timed(*args, arr)
     _raise(st, "wna16_fused_moe")
+    return out
+
+
+def fused_moe_noalloc(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tensor,
+                      w13_zeros: Optional[torch.Tensor], w2_q: torch.Tensor, w2_scales: torch.Tensor,
+                      w2_zeros: Optional[torch.Tensor], topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                      bits: int, group_size: int, out: torch.Tensor, block: int = 0, split_k: int = 0,
+                      stream=None) -> torch.Tensor:
+    """The fused layer through ``wna16_fused_moe_noalloc``: no workspace is passed
+    and none is allocated (the library's fixed scratch area is used; see the
+    header). ``out`` [M, H] must be given, so this call allocates nothing either."""
+    _check(hidden, "hidden", (torch.float16, torch.bfloat16))
+    dev = hidden.device
+    M, H = hidden.shape
+    E, twoI, _ = w13_q.shape
+    I = twoI // 2
+    for t, n in ((w13_q, "w13_q"), (w2_q, "w2_q"), (topk_ids, "topk_ids")):
+        _check(t, n, torch.int32, device=dev)
+    _check(w13_scales, "w13_scales", (torch.float16, torch.bfloat16), device=dev)
+    _check(w2_scales, "w2_scales", w13_scales.dtype, device=dev)
+    _check(topk_weights, "topk_weights", torch.float32, device=dev)
+    _check(out, "out", hidden.dtype, (M, H), dev)
+    topk = topk_ids.shape[1]
+    st = load().wna16_fused_moe_noalloc(
+        _ptr(hidden), _DTYPE[hidden.dtype], M, H, I, E, topk, _ptr(w13_q), _ptr(w13_scales),
+        _ptr(w13_zeros), _ptr(w2_q), _ptr(w2_scales), _ptr(w2_zeros), _DTYPE[w13_scales.dtype], bits,
+        group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out), block, split_k, _stream(stream))
+    _raise(st, "wna16_fused_moe_noalloc")
     return out
 
 
