@@ -240,14 +240,14 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
       const uint32_t stage_tx = W_BYTES + SG * 256 + (a.has_zeros ? SG * (kTileRows / PF) * 4 : 0) + BST;
       const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
       const uint64_t pol_b = l2_policy_evict_last();   // token rows: re-read by every row tile
-      int it = 0;
+      int it = 0, s = 0;
+      uint32_t e_phase = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const Unit w = decode_unit(u, nb, a);
         const int e = unit_expert(a, w.blk);
         bool ok = true;
         for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
-          const int s = it % NS;
-          if (!wait_bar(&empty[s], ((it / NS) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+          if (!wait_bar(&empty[s], e_phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], stage_tx);
           uint8_t* dst = wring + s * WST;
           const int ys = e * a.groups + (kt * kTileK) / a.G;
@@ -267,6 +267,10 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           for (int c = 0; c < kTileK / kChunkK; ++c)
             tma_load_2d(bring + s * BST + c * NT * 128, &tm_b, &full[s], kt * kTileK + c * kChunkK, w.blk * NT,
                         pol_b);
+          if (++s == NS) {
+            s = 0;
+            e_phase ^= 1u;
+          }
         }
         if (!ok) break;
       }
@@ -275,9 +279,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Kept lean (wrapping counters, precomputed descriptors, unrolled MMAs):
+    // this single thread issues every MMA of the CTA and shares its SM
+    // sub-partition with dequant warps.
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(ACT, NT);
-      int it = 0, uc = 0;
+      const uint32_t a_base = tmem + NACC * NT;
+      const uint64_t chunk_step = static_cast<uint64_t>((NT * 128) >> 4);  // next 64-wide K chunk
+      int s = 0, slot = 0, uc = 0;
+      uint32_t a_phase = 0;
       bool issued = false;
       for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
         const Unit w = decode_unit(u, nb, a);
@@ -286,21 +296,28 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * NT;
         bool ok = true;
-        for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
-          const int s = it % NS;
-          const int slot = it % NA;
+        for (int kt = w.kt0; kt < w.kt1; ++kt) {
           // afull implies the stage landed (the dequant warps waited on full[s])
-          if (!wait_bar(&afull[slot], (it / NA) & 1, abort_flag, a.status)) { ok = false; break; }
+          if (!wait_bar(&afull[slot], a_phase, abort_flag, a.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_tmem = tmem + NACC * NT + slot * kASlotCols;
-          const uint64_t b_desc = smem_desc_sw128(smem_u32(bring + s * BST));
-          const uint64_t chunk_step = static_cast<uint64_t>((NT * 128) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk)
-            mma_ts(d_tmem, a_tmem + kk * 8, b_desc + (kk / 4) * chunk_step + 2 * (kk % 4) /* 32 B per K=16 */,
-                   idesc, (kt > w.kt0 || kk > 0) ? 1u : 0u);
+          const uint32_t at = a_base + slot * kASlotCols;
+          const uint64_t b0 = smem_desc_sw128(smem_u32(bring + s * BST));
+          const uint64_t b1 = b0 + chunk_step;
+          mma_ts(d_tmem, at, b0, idesc, kt > w.kt0 ? 1u : 0u);
+          mma_ts_acc(d_tmem, at + 8, b0 + 2, idesc);  // +32 B per K=16 step
+          mma_ts_acc(d_tmem, at + 16, b0 + 4, idesc);
+          mma_ts_acc(d_tmem, at + 24, b0 + 6, idesc);
+          mma_ts_acc(d_tmem, at + 32, b1, idesc);
+          mma_ts_acc(d_tmem, at + 40, b1 + 2, idesc);
+          mma_ts_acc(d_tmem, at + 48, b1 + 4, idesc);
+          mma_ts_acc(d_tmem, at + 56, b1 + 6, idesc);
           mma_commit(&empty[s]);
           issued = true;
+          if (++s == NS) s = 0;
+          if (++slot == NA) {
+            slot = 0;
+            a_phase ^= 1u;
+          }
         }
         if (!ok) break;
         mma_commit(&accfull[acc]);
@@ -386,20 +403,32 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
       hrow = srow;
     }
     const uint32_t t_lane = (q * 32) << 16;
-    int it = 0;
+    // Running positions (stage index it, its ring slot s and phase, A slot,
+    // and the stage it - NA whose completion frees that A slot), advanced for
+    // every stage so both warpgroups agree on them.
+    int it = 0, s = 0, slot = 0, ps = NS - NA;  // ps = (it - NA) mod NS
+    uint32_t f_phase = 0, p_phase = 1;          // p_phase: phase of stage it - NA (unused while it < NA)
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = decode_unit(u, nb, a);
       bool ok = true;
       for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
-        if ((it & 1) != grp) continue;
-        const int s = it % NS;
-        const int slot = it % NA;
-        if (!warp_wait(&full[s], (it / NS) & 1, abort_flag, a.status)) { ok = false; break; }
-        if (it >= NA) {
-          const int prev = it - NA;
-          if (!warp_wait(&empty[prev % NS], (prev / NS) & 1, abort_flag, a.status)) { ok = false; break; }
+        const int cs = s, cslot = slot, cps = ps;
+        const uint32_t cf = f_phase, cp = p_phase;
+        if (++s == NS) {
+          s = 0;
+          f_phase ^= 1u;
         }
-        const uint8_t* st = wring + s * WST;
+        if (++slot == NA) slot = 0;
+        if (++ps == NS) {
+          ps = 0;
+          p_phase ^= 1u;
+        }
+        if ((it & 1) != grp) continue;
+        if (!warp_wait(&full[cs], cf, abort_flag, a.status)) { ok = false; break; }
+        if (it >= NA) {
+          if (!warp_wait(&empty[cps], cp, abort_flag, a.status)) { ok = false; break; }
+        }
+        const uint8_t* st = wring + cs * WST;
         // scale and zero point of each 64-wide chunk of the stage (group rows 0/1 when G = 64)
         uint32_t sbits[2], zero[2];
 #pragma unroll
@@ -428,12 +457,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           }
           uint32_t outv[16];
           Dequant<BITS, ACT, SCL>::run(wv, zero[h >> 1], sbits[h >> 1], outv);
-          tmem_st16(tmem + t_lane + NACC * NT + slot * kASlotCols + h * 16, outv);
+          tmem_st16(tmem + t_lane + NACC * NT + cslot * kASlotCols + h * 16, outv);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[slot]);
+        if (lane == 0) mbar_arrive(&afull[cslot]);
       }
       if (!ok) break;
     }
