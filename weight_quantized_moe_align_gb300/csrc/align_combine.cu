@@ -153,11 +153,13 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
 }
 
 // Copies the hidden row of every routed pair to its expert-sorted slot:
-// x_sorted[slot_of_pair[p]] = hidden[p / topk] (16-byte vectors). Padded slots
-// are not written: they only feed MMA columns whose results are discarded.
+// x_sorted[slot_of_pair[p]] = hidden[p / topk] (16-byte vectors of 8 elements).
+// With `permute` (int4 weights) each vector is stored in the GEMM's K order
+// 0,4,1,5,2,6,3,7. Padded slots are not written: they only feed MMA columns
+// whose results are discarded.
 __global__ void __launch_bounds__(256)
     moe_gather_kernel(const uint4* __restrict__ hidden, const int32_t* __restrict__ ids,
-                      const int32_t* __restrict__ slot_of_pair, int P, int topk, int E, int h8,
+                      const int32_t* __restrict__ slot_of_pair, int P, int topk, int E, int h8, int permute,
                       uint4* __restrict__ x_sorted) {
   const long long n = static_cast<long long>(P) * h8;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
@@ -166,7 +168,15 @@ __global__ void __launch_bounds__(256)
     const int c = static_cast<int>(idx % h8);
     const int e = ids[p];
     if (e < 0 || e >= E) continue;
-    x_sorted[static_cast<long long>(slot_of_pair[p]) * h8 + c] = hidden[static_cast<long long>(p / topk) * h8 + c];
+    uint4 v = hidden[static_cast<long long>(p / topk) * h8 + c];
+    if (permute) {  // (x0 x1)(x2 x3)(x4 x5)(x6 x7) -> (x0 x4)(x1 x5)(x2 x6)(x3 x7)
+      const uint4 u = v;
+      v.x = __byte_perm(u.x, u.z, 0x5410);
+      v.y = __byte_perm(u.x, u.z, 0x7632);
+      v.z = __byte_perm(u.y, u.w, 0x5410);
+      v.w = __byte_perm(u.y, u.w, 0x7632);
+    }
+    x_sorted[static_cast<long long>(slot_of_pair[p]) * h8 + c] = v;
   }
 }
 
@@ -215,7 +225,7 @@ cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, i
 }
 
 cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
-                          int topk, int E, int H, int max_ctas, void* x_sorted, cudaStream_t stream) {
+                          int topk, int E, int H, int permute, int max_ctas, void* x_sorted, cudaStream_t stream) {
   const int h8 = H / 8;
   const long long n = static_cast<long long>(P) * h8;
   const int threads = 256;
@@ -223,7 +233,7 @@ cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t*
   const unsigned blocks = static_cast<unsigned>(want < max_ctas ? want : max_ctas);
   if (blocks == 0) return cudaSuccess;
   moe_gather_kernel<<<blocks, threads, 0, stream>>>(static_cast<const uint4*>(hidden), ids, slot_of_pair, P,
-                                                    topk, E, h8, static_cast<uint4*>(x_sorted));
+                                                    topk, E, h8, permute, static_cast<uint4*>(x_sorted));
   return cudaGetLastError();
 }
 

@@ -12,12 +12,14 @@ namespace wna16 {
 //   1      tcgen05 MMA issuer, owner of the TMEM allocation
 //   2..5   epilogue (TMEM -> registers -> global); lane quarter = warp % 4
 //   6..13  dequantizers, two stage-parallel warpgroups (shared -> registers -> TMEM)
-// Token tiles up to 64 run two CTAs per SM (256 TMEM columns, <= 112 KB of
-// shared memory each) so two MMA streams overlap on the SM; larger tiles take
-// the whole SM.
-constexpr int kGemmThreads = 448;
-constexpr int kDequantWarps = 8;
+// A lean layout (producer, MMA issuer, 4 dequant warps that also run the
+// epilogue) fits four CTAs per SM for int4 token tiles up to 32 (128 TMEM
+// columns, <= 56 KB of shared memory each): four MMA-issuing threads share the
+// tensor core. Other tiles up to 64 run two CTAs per SM of the full layout
+// (256 TMEM columns, <= 112 KB each); larger tiles take the whole SM.
+constexpr int kDequantWarps = 8;   // two warpgroups (LEAN = 0); LEAN = 1 uses one
 constexpr int kEpilogueWarps = 4;
+__host__ __device__ constexpr int gemm_threads(int lean) { return lean ? 6 * 32 : 14 * 32; }
 
 constexpr int kTileK = 128;      // K elements per pipeline stage
 constexpr int kChunkK = 64;      // K elements per 128-byte swizzle atom of the token tile
@@ -26,6 +28,17 @@ constexpr int kGateUpRows = 64;  // gate/up GEMM: 64 gate + 64 up rows per tile
 constexpr int kMaxStages = 16;
 constexpr int kMaxASlots = 8;
 constexpr int kASlotCols = kTileK / 2;  // TMEM columns of one stage's A operand (2 halves per column)
+
+// int4 operands run with K permuted inside every group of 8 elements: stored
+// position of element k is 2k for k < 4 and 2(k - 4) + 1 for k >= 4 (order
+// 0,4,1,5,2,6,3,7), which lets one lop3 extract a pair of codes. The token
+// operands (gathered hidden rows, act cache) are written in that order; the
+// product does not change since both operands share it.
+template <int BITS>
+constexpr bool kPermuteK = BITS == 4;
+__host__ __device__ constexpr int permute_k8(int k) {
+  return (k & ~7) | ((k & 7) < 4 ? 2 * (k & 7) : 2 * ((k & 7) - 4) + 1);
+}
 
 struct GemmArgs {
   const int32_t* sorted_ids;   // [cap]

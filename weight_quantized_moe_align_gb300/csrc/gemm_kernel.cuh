@@ -74,36 +74,45 @@ __device__ __forceinline__ float code_minus_zero(uint32_t code, float magic_plus
   return __uint_as_float(0x4B000000u | code) - magic_plus_zero;
 }
 
-// Dequantizes 32 consecutive K elements of one weight row into 16 packed pairs
-// (element 2c in the low half of out[c]). Every value is round((u - z) * s) to
-// the activation dtype, rounded once: the product of a <= 8-bit integer and a
-// 16-bit scale is exact in fp32 and in the half-precision fast paths the
-// subtraction is exact and the multiply rounds once.
+// Dequantizes 32 consecutive K elements of one weight row into 16 packed
+// pairs. int8: natural order, out[c] = (element 2c, element 2c+1). int4: each
+// word of 8 codes k0..k7 yields the pairs (k0,k4), (k1,k5), (k2,k6), (k3,k7),
+// so the operand's K order inside every group of 8 is 0,4,1,5,2,6,3,7 (the
+// token operand is stored in the same order; see kPermuteK). Every value is
+// round((u - z) * s) to the activation dtype, rounded once: the subtraction of
+// the magic-number forms is exact and the multiply rounds once, and in the fp32
+// path the product of a <= 8-bit integer and a 16-bit scale is exact.
 template <int BITS, int ACT, int SCL>
 struct Dequant {
   static __device__ __forceinline__ void run(const uint32_t* w, uint32_t zero, uint32_t scale_bits,
                                              uint32_t (&out)[16]) {
-    if constexpr (BITS == 4 && ACT == SCL) {
-      // Magic-exponent conversion: a nibble OR-ed into the mantissa of
-      // 1024.0 (fp16) or 128.0 (bf16) is exactly 1024+u / 128+u.
-      constexpr uint32_t kMagic = ACT == 0 ? 0x64006400u : 0x43004300u;
-      const float base = ACT == 0 ? 1024.f : 128.f;
-      uint32_t zc, sc;
-      {
-        const uint32_t zb = pack2_rn<ACT>(base + float(zero), base + float(zero));
-        zc = zb;
-        sc = (scale_bits & 0xFFFFu) | (scale_bits << 16);
-      }
+    if constexpr (BITS == 4 && ACT == 0 && SCL == 0) {
+      // A nibble OR-ed into bits 0-3 of 1024.0 is exactly 1024 + u; one OR-ed
+      // into bits 4-7 of 64.0 is exactly 64 + u. One lop3 per pair extracts
+      // (k_j, k_j+4) from bits 4j.. of the word and of the word >> 8.
+      const uint32_t z_lo = pack2_rn<0>(1024.f + float(zero), 1024.f + float(zero));
+      const uint32_t z_hi = pack2_rn<0>(64.f + float(zero), 64.f + float(zero));
+      const uint32_t sc = (scale_bits & 0xFFFFu) | (scale_bits << 16);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t x = w[i];
-        const uint32_t xs = x >> 4;
+        const uint32_t x8 = x >> 8;
+        out[i * 4 + 0] = hsub_hmul<0>(lop3_and_or(x, 0x000F000Fu, 0x64006400u), z_lo, sc);   // k0, k4
+        out[i * 4 + 1] = hsub_hmul<0>(lop3_and_or(x, 0x00F000F0u, 0x54005400u), z_hi, sc);   // k1, k5
+        out[i * 4 + 2] = hsub_hmul<0>(lop3_and_or(x8, 0x000F000Fu, 0x64006400u), z_lo, sc);  // k2, k6
+        out[i * 4 + 3] = hsub_hmul<0>(lop3_and_or(x8, 0x00F000F0u, 0x54005400u), z_hi, sc);  // k3, k7
+      }
+    } else if constexpr (BITS == 4 && ACT == 1 && SCL == 1) {
+      // bf16: a nibble in bits 0-3 of 128.0 is exactly 128 + u (bits 4-7 would
+      // reach the exponent), so each pair is shifted down first.
+      const uint32_t zc = pack2_rn<1>(128.f + float(zero), 128.f + float(zero));
+      const uint32_t sc = (scale_bits & 0xFFFFu) | (scale_bits << 16);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // byte0 <- low nibble of byte j (element 2j), byte2 <- high nibble (2j+1)
-          const uint32_t t = __byte_perm(x, xs, j | ((j + 4) << 8));
-          out[i * 4 + j] = hsub_hmul<ACT>(lop3_and_or(t, 0x000F000Fu, kMagic), zc, sc);
-        }
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t x = w[i];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          out[i * 4 + j] = hsub_hmul<1>(lop3_and_or(x >> (4 * j), 0x000F000Fu, 0x43004300u), zc, sc);
       }
     } else if constexpr (BITS == 8 && ACT == 0 && SCL == 0) {
       const uint32_t zc = pack2_rn<0>(1024.f + float(zero), 1024.f + float(zero));
@@ -120,16 +129,24 @@ struct Dequant {
       const float s = SCL == 0 ? __half2float(__ushort_as_half((unsigned short)scale_bits))
                                : __bfloat162float(__ushort_as_bfloat16((unsigned short)scale_bits));
       const float mz = 8388608.f + float(zero);
-      constexpr int PF = 32 / BITS;
       constexpr uint32_t MASK = (1u << BITS) - 1;
 #pragma unroll
       for (int i = 0; i < BITS; ++i) {  // 4 words of int4 or 8 words of int8
         const uint32_t x = w[i];
+        if constexpr (BITS == 4) {
 #pragma unroll
-        for (int c = 0; c < PF; c += 2) {
-          const float f0 = code_minus_zero((x >> (BITS * c)) & MASK, mz) * s;
-          const float f1 = code_minus_zero((x >> (BITS * (c + 1))) & MASK, mz) * s;
-          out[(i * PF + c) / 2] = pack2_rn<ACT>(f0, f1);
+          for (int j = 0; j < 4; ++j) {  // pairs (k_j, k_j+4)
+            const float f0 = code_minus_zero((x >> (4 * j)) & MASK, mz) * s;
+            const float f1 = code_minus_zero((x >> (4 * (j + 4))) & MASK, mz) * s;
+            out[i * 4 + j] = pack2_rn<ACT>(f0, f1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; c += 2) {
+            const float f0 = code_minus_zero((x >> (8 * c)) & MASK, mz) * s;
+            const float f1 = code_minus_zero((x >> (8 * (c + 1))) & MASK, mz) * s;
+            out[(i * 4 + c) / 2] = pack2_rn<ACT>(f0, f1);
+          }
         }
       }
     }
@@ -164,8 +181,72 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
-template <int BITS, int ACT, int SCL, int GEMM>
-__global__ void __launch_bounds__(kGemmThreads, 2)
+// Epilogue of one work unit, run by four warps covering the four TMEM lane
+// quarters: waits for the unit's accumulator, reads it 16 token columns at a
+// time and writes silu(gate) * up to the act cache (gate/up GEMM) or the
+// top-k-weighted fp32 row of each (token, slot) pair (down GEMM), then frees
+// the accumulator. Returns false if the wait gave up.
+template <int BITS, int ACT, int GEMM>
+__device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, uint32_t tmem, int acc,
+                                              uint32_t acc_phase, uint64_t* accfull, uint64_t* accempty,
+                                              volatile int* abort_flag, int q, int lane) {
+  const int NT = a.block;
+  if (!warp_wait(&accfull[acc], acc_phase, abort_flag, a.status)) return false;
+  tc_fence_after();
+  const uint32_t t_base = tmem + ((q * 32) << 16) + acc * NT;
+  for (int c0 = 0; c0 < NT; c0 += 16) {
+    uint32_t v[16];
+    tmem_ld16(t_base + c0, v);
+    tmem_ld_wait();
+    if (GEMM == 1) {
+      // Lanes 0-15 of this quarter hold gate rows, lanes 16-31 the up rows of
+      // the same 16 features; swap halves so each lane owns 8 (feature, token)
+      // pairs with both values.
+      using T = typename Act<ACT>::T;
+      T* act = reinterpret_cast<T*>(a.out);
+      const bool lo = lane < 16;
+      const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t mine = lo ? v[j] : v[j + 8];
+        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, lo ? v[j + 8] : v[j], 16);
+        const float g = __uint_as_float(lo ? mine : other);
+        const float up = __uint_as_float(lo ? other : mine);
+        const float silu = g / (1.0f + __expf(-g));
+        const int col = c0 + (lo ? j : j + 8);
+        const size_t row = static_cast<size_t>(w.blk) * NT + col;
+        const int fp = kPermuteK<BITS> ? permute_k8(f) : f;  // the down GEMM's K order
+        if constexpr (ACT == 0)
+          act[row * a.I + fp] = __float2half_rn(silu * up);
+        else
+          act[row * a.I + fp] = __float2bfloat16_rn(silu * up);
+      }
+    } else {
+      float* slab = reinterpret_cast<float*>(a.out);
+      const int h = w.tile * kTileRows + q * 32 + lane;
+      const int my_pid = a.sorted_ids[w.blk * NT + c0 + (lane & 15)];
+      const float my_w = (my_pid >= 0 && my_pid < a.P) ? a.topk_w[my_pid] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int pid = __shfl_sync(0xFFFFFFFFu, my_pid, j);
+        const float tw = __shfl_sync(0xFFFFFFFFu, my_w, j);
+        if (pid >= 0 && pid < a.P && h < a.N)
+          slab[(static_cast<size_t>(w.sp) * a.P + pid) * a.N + h] = __uint_as_float(v[j]) * tw;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&accempty[acc]);
+  return true;
+}
+
+// LEAN = 0: 14 warps (producer, MMA issuer, 4 epilogue warps, two dequant
+// warpgroups), two CTAs per SM. LEAN = 1: 6 warps (producer, MMA issuer, one
+// dequant warpgroup that also runs the epilogue), four CTAs per SM, so four
+// MMA-issuing threads share the SM's tensor core (decode-sized token tiles).
+template <int BITS, int ACT, int SCL, int GEMM, int LEAN>
+__global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
                     const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_b,
                     const GemmArgs a) {
@@ -327,69 +408,25 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         wait_bar_drain(drain, 0);
       }
     }
-  } else if (warp < 2 + kEpilogueWarps) {
+  } else if (!LEAN && warp < 2 + kEpilogueWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int uc = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
       const Unit w = decode_unit(u, nb, a);
-      const int acc = uc % NACC;
-      if (!warp_wait(&accfull[acc], (uc / NACC) & 1, abort_flag, a.status)) break;
-      tc_fence_after();
-      const uint32_t t_base = tmem + ((q * 32) << 16) + acc * NT;
-      for (int c0 = 0; c0 < NT; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(t_base + c0, v);
-        tmem_ld_wait();
-        if (GEMM == 1) {
-          // Lanes 0-15 of this quarter hold gate rows, lanes 16-31 the up rows of
-          // the same 16 features; swap halves so each lane owns 8 (feature, token)
-          // pairs with both values.
-          using T = typename Act<ACT>::T;
-          T* act = reinterpret_cast<T*>(a.out);
-          const bool lo = lane < 16;
-          const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t mine = lo ? v[j] : v[j + 8];
-            const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, lo ? v[j + 8] : v[j], 16);
-            const float g = __uint_as_float(lo ? mine : other);
-            const float up = __uint_as_float(lo ? other : mine);
-            const float silu = g / (1.0f + __expf(-g));
-            const int col = c0 + (lo ? j : j + 8);
-            const size_t row = static_cast<size_t>(w.blk) * NT + col;
-            if constexpr (ACT == 0)
-              act[row * a.I + f] = __float2half_rn(silu * up);
-            else
-              act[row * a.I + f] = __float2bfloat16_rn(silu * up);
-          }
-        } else {
-          float* slab = reinterpret_cast<float*>(a.out);
-          const int h = w.tile * kTileRows + q * 32 + lane;
-          const int my_pid = a.sorted_ids[w.blk * NT + c0 + (lane & 15)];
-          const float my_w = (my_pid >= 0 && my_pid < a.P) ? a.topk_w[my_pid] : 0.f;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int pid = __shfl_sync(0xFFFFFFFFu, my_pid, j);
-            const float tw = __shfl_sync(0xFFFFFFFFu, my_w, j);
-            if (pid >= 0 && pid < a.P && h < a.N)
-              slab[(static_cast<size_t>(w.sp) * a.P + pid) * a.N + h] = __uint_as_float(v[j]) * tw;
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&accempty[acc]);
+      if (!epilogue_unit<BITS, ACT, GEMM>(a, w, tmem, uc % NACC, (uc / NACC) & 1, accfull, accempty, abort_flag, q, lane))
+        break;
     }
   } else {
     // ------------------------------------------------------------ dequantizers
-    // Two warpgroups, stage-parallel: warpgroup g dequantizes the stages whose
-    // running index is congruent to g mod 2, one full 128-element K row per
-    // thread (thread = TMEM lane = weight row), so two stages are in flight.
+    // LEAN = 0: two warpgroups, stage-parallel: warpgroup g dequantizes the
+    // stages whose running index is congruent to g mod 2, so two stages are in
+    // flight. LEAN = 1: one warpgroup takes every stage. One full 128-element K
+    // row per thread (thread = TMEM lane = weight row).
     // A slot it % NA is free once the MMAs of stage it - NA completed, which is
     // the completion of that stage's `empty` phase.
     const int q = warp & 3;
-    const int grp = (warp - 2 - kEpilogueWarps) >> 2;
+    const int grp = LEAN ? 0 : (warp - 2 - kEpilogueWarps) >> 2;
     // Weight row (in the stage's smem tile) of this thread's TMEM lane. Gate/up:
     // lanes 0-15 of quarter q take gate rows 16q.., lanes 16-31 the up rows of
     // the same features, so the epilogue finds gate and up in one warp.
@@ -407,6 +444,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     // and the stage it - NA whose completion frees that A slot), advanced for
     // every stage so both warpgroups agree on them.
     int it = 0, s = 0, slot = 0, ps = NS - NA;  // ps = (it - NA) mod NS
+    int uc = 0;                                 // units finished (epilogue count, LEAN)
     uint32_t f_phase = 0, p_phase = 1;          // p_phase: phase of stage it - NA (unused while it < NA)
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = decode_unit(u, nb, a);
@@ -423,7 +461,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
           ps = 0;
           p_phase ^= 1u;
         }
-        if ((it & 1) != grp) continue;
+        if (!LEAN && (it & 1) != grp) continue;
         if (!warp_wait(&full[cs], cf, abort_flag, a.status)) { ok = false; break; }
         if (it >= NA) {
           if (!warp_wait(&empty[cps], cp, abort_flag, a.status)) { ok = false; break; }
@@ -443,13 +481,17 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             zero[c] = (reinterpret_cast<const uint32_t*>(st + Z_OFF)[zi] >> (BITS * (hrow % PF))) & ZMASK;
           }
         }
+        // Code rows are TMA-swizzled (64-byte rows: 16-byte chunk c of row r sits at
+        // chunk c ^ ((r >> 1) & 3); 128-byte rows: at c ^ (r & 7)), so the 8 lanes
+        // of a load phase, 8 consecutive rows, hit distinct banks.
         const uint4* src = reinterpret_cast<const uint4*>(st + srow * KW * 4);
+        const int swz = BITS == 4 ? ((srow >> 1) & 3) : (srow & 7);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {  // four 32-element quarters of the row
           uint32_t wv[BITS];
 #pragma unroll
           for (int i = 0; i < BITS / 4; ++i) {
-            const uint4 x = src[h * (BITS / 4) + i];
+            const uint4 x = src[(h * (BITS / 4) + i) ^ swz];
             wv[4 * i + 0] = x.x;
             wv[4 * i + 1] = x.y;
             wv[4 * i + 2] = x.z;
@@ -465,6 +507,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         if (lane == 0) mbar_arrive(&afull[cslot]);
       }
       if (!ok) break;
+      if (LEAN) {
+        // this warpgroup also runs the epilogue, right after the unit's last stage
+        if (!epilogue_unit<BITS, ACT, GEMM>(a, w, tmem, uc % NACC, (uc / NACC) & 1, accfull, accempty, abort_flag, q,
+                                      lane))
+          break;
+        ++uc;
+      }
     }
   }
 

@@ -6,10 +6,10 @@
 namespace wna16 {
 
 // gemm: 1 = gate/up + silu*up epilogue, 2 = down + top-k weight epilogue.
-cudaError_t launch_gemm_w4(int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
+cudaError_t launch_gemm_w4(int act, int scl, int gemm, int lean, dim3 grid, size_t smem, cudaStream_t stream,
                            const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                            const CUtensorMap& b, const GemmArgs& a);
-cudaError_t launch_gemm_w8(int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
+cudaError_t launch_gemm_w8(int act, int scl, int gemm, int lean, dim3 grid, size_t smem, cudaStream_t stream,
                            const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                            const CUtensorMap& b, const GemmArgs& a);
 
@@ -17,7 +17,8 @@ cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, i
                          int32_t* expert_ids, int32_t* num_post_pad, int32_t* counts,
                          int32_t* status, int32_t* slot_of_pair, cudaStream_t stream);
 cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
-                          int topk, int E, int H, int max_ctas, void* x_sorted, cudaStream_t stream);
+                          int topk, int E, int H, int permute, int max_ctas, void* x_sorted,
+                          cudaStream_t stream);
 cudaError_t launch_combine(const float* slab, const int32_t* ids, int M, int H, int topk, int E,
                            int split, int act_dtype, void* out, cudaStream_t stream);
 

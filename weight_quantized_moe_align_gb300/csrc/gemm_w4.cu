@@ -6,10 +6,10 @@ namespace wna16 {
 
 namespace {
 
-template <int ACT, int SCL, int GEMM>
+template <int ACT, int SCL, int GEMM, int LEAN>
 cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t stream, const CUtensorMap& q,
                        const CUtensorMap& s, const CUtensorMap& z, const CUtensorMap& b, const GemmArgs& a) {
-  auto* fn = moe_gemm_kernel<4, ACT, SCL, GEMM>;
+  auto* fn = moe_gemm_kernel<4, ACT, SCL, GEMM, LEAN>;
   // The opt-in shared-memory limit is per function and context; set it at most
   // once per device.
   static bool configured[64] = {};
@@ -21,27 +21,31 @@ cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t stream, const CUtens
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  fn<<<grid, kGemmThreads, smem, stream>>>(q, s, z, b, a);
+  fn<<<grid, gemm_threads(LEAN), smem, stream>>>(q, s, z, b, a);
   return cudaGetLastError();
 }
 
-template <int GEMM>
+template <int GEMM, int LEAN>
 cudaError_t by_dtype(int act, int scl, dim3 grid, size_t smem, cudaStream_t stream,
                      const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                      const CUtensorMap& b, const GemmArgs& a) {
-  if (act == 0 && scl == 0) return launch_one<0, 0, GEMM>(grid, smem, stream, q, s, z, b, a);
-  if (act == 0 && scl == 1) return launch_one<0, 1, GEMM>(grid, smem, stream, q, s, z, b, a);
-  if (act == 1 && scl == 0) return launch_one<1, 0, GEMM>(grid, smem, stream, q, s, z, b, a);
-  return launch_one<1, 1, GEMM>(grid, smem, stream, q, s, z, b, a);
+  if (act == 0 && scl == 0) return launch_one<0, 0, GEMM, LEAN>(grid, smem, stream, q, s, z, b, a);
+  if (act == 0 && scl == 1) return launch_one<0, 1, GEMM, LEAN>(grid, smem, stream, q, s, z, b, a);
+  if (act == 1 && scl == 0) return launch_one<1, 0, GEMM, LEAN>(grid, smem, stream, q, s, z, b, a);
+  return launch_one<1, 1, GEMM, LEAN>(grid, smem, stream, q, s, z, b, a);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_w4(int act, int scl, int gemm, dim3 grid, size_t smem,
+cudaError_t launch_gemm_w4(int act, int scl, int gemm, int lean, dim3 grid, size_t smem,
                             cudaStream_t stream, const CUtensorMap& q, const CUtensorMap& s,
                             const CUtensorMap& z, const CUtensorMap& b, const GemmArgs& a) {
-  if (gemm == 1) return by_dtype<1>(act, scl, grid, smem, stream, q, s, z, b, a);
-  return by_dtype<2>(act, scl, grid, smem, stream, q, s, z, b, a);
+  if (lean) {
+    if (gemm == 1) return by_dtype<1, 1>(act, scl, grid, smem, stream, q, s, z, b, a);
+    return by_dtype<2, 1>(act, scl, grid, smem, stream, q, s, z, b, a);
+  }
+  if (gemm == 1) return by_dtype<1, 0>(act, scl, grid, smem, stream, q, s, z, b, a);
+  return by_dtype<2, 0>(act, scl, grid, smem, stream, q, s, z, b, a);
 }
 
 }  // namespace wna16

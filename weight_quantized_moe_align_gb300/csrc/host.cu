@@ -18,6 +18,7 @@ namespace {
 
 constexpr int kMaxSmem = 232448;   // opt-in dynamic shared memory per CTA on sm_103a
 constexpr int kHalfSmem = 112 * 1024;  // two CTAs per SM
+constexpr int kQuarterSmem = 55 * 1024;  // four CTAs per SM
 constexpr int kMinSmem = 120 * 1024;   // a whole-SM CTA (512 TMEM columns) runs alone on its SM
 
 bool is_pow2(long long v) { return v > 0 && (v & (v - 1)) == 0; }
@@ -50,27 +51,35 @@ int choose_block_impl(int64_t M, int topk, int E) {
   return b;
 }
 
-// Pipeline shape of one GEMM launch for a token tile of `block`. Token tiles up
-// to 64 use half of the SM (256 TMEM columns, <= 112 KB of shared memory) so two
-// CTAs, and so two MMA streams, share each SM; larger tiles take the whole SM.
+// Pipeline shape of one GEMM launch for a token tile of `block`.
+//  * lean layout (when selected): four CTAs per SM (128 TMEM columns: one
+//    accumulator and one A slot; <= 55 KB of shared memory each), four
+//    MMA-issuing threads sharing the tensor core.
+//  * tiles up to 64: two CTAs per SM of the full layout (256 TMEM columns,
+//    <= 112 KB of shared memory).
+//  * larger tiles: one CTA per SM.
 struct Pipe {
-  int stages, aslots, acc, ctas_per_sm;
+  int stages, aslots, acc, ctas_per_sm, lean;
   uint32_t tmem_cols;
   size_t smem;
 };
 
 Pipe pipe_for(int bits, int block) {
   Pipe p;
-  const bool half_sm = block <= 64;
-  p.ctas_per_sm = half_sm ? 2 : 1;
-  p.tmem_cols = half_sm ? 256 : 512;
-  const int smem_cap = half_sm ? kHalfSmem : kMaxSmem;
-  p.acc = (2 * block + 2 * kASlotCols <= static_cast<int>(p.tmem_cols)) ? 2 : 1;
+  // The lean layout (LEAN = 1) is built and selectable here; measured on
+  // Mixtral-8x7B decode it was slower than two full-layout CTAs per SM (its
+  // single A slot serialises dequant and MMA inside each CTA), so it is off.
+  p.lean = 0;
+  const bool half_sm = !p.lean && block <= 64;
+  p.ctas_per_sm = p.lean ? 4 : (half_sm ? 2 : 1);
+  p.tmem_cols = p.lean ? 128 : (half_sm ? 256 : 512);
+  const int smem_cap = p.lean ? kQuarterSmem : (half_sm ? kHalfSmem : kMaxSmem);
+  p.acc = p.lean ? 1 : ((2 * block + 2 * kASlotCols <= static_cast<int>(p.tmem_cols)) ? 2 : 1);
   p.stages = kMaxStages;
   while (p.stages > 2 && gemm_smem_bytes(bits, block, p.stages) > smem_cap) --p.stages;
   p.aslots = std::min({kMaxASlots, (static_cast<int>(p.tmem_cols) - p.acc * block) / kASlotCols, p.stages - 1});
   p.smem = gemm_smem_bytes(bits, block, p.stages);
-  if (!half_sm) p.smem = std::max<size_t>(p.smem, kMinSmem);
+  if (p.ctas_per_sm == 1) p.smem = std::max<size_t>(p.smem, kMinSmem);
   return p;
 }
 
@@ -158,13 +167,16 @@ bool make_gemm_maps(GemmMaps* g, const int32_t* q, const void* s, const int32_t*
   const uint64_t groups = K / G;
   const uint32_t sg = G < kTileK ? kTileK / G : 1;
   const uint32_t kw = kTileK / pf;
+  // Code rows of a stage are 64 B (int4) or 128 B (int8): swizzled so that the
+  // dequant warps' 16-byte reads of 8 consecutive rows hit distinct banks.
+  const CUtensorMapSwizzle qswz = bits == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   std::memset(g, 0, sizeof(*g));
   if (gate_up) {
     const uint64_t I = N / 2;
     const uint64_t qd[3] = {static_cast<uint64_t>(K / pf), I, 2ull * E};
     const uint64_t qs[2] = {static_cast<uint64_t>(K / pf) * 4, I * (K / pf) * 4};
     const uint32_t qb[3] = {kw, kGateUpRows, 2};
-    if (!make_map(&g->q, CU_TENSOR_MAP_DATA_TYPE_INT32, q, 3, qd, qs, qb)) return false;
+    if (!make_map(&g->q, CU_TENSOR_MAP_DATA_TYPE_INT32, q, 3, qd, qs, qb, qswz)) return false;
     const uint64_t sd[3] = {I, 2, E * groups};
     const uint64_t ss[2] = {I * 2, 2 * I * 2};
     const uint32_t sb[3] = {kGateUpRows, 2, sg};
@@ -179,7 +191,7 @@ bool make_gemm_maps(GemmMaps* g, const int32_t* q, const void* s, const int32_t*
     const uint64_t qd[2] = {static_cast<uint64_t>(K / pf), static_cast<uint64_t>(E) * N};
     const uint64_t qs[1] = {static_cast<uint64_t>(K / pf) * 4};
     const uint32_t qb[2] = {kw, kTileRows};
-    if (!make_map(&g->q, CU_TENSOR_MAP_DATA_TYPE_INT32, q, 2, qd, qs, qb)) return false;
+    if (!make_map(&g->q, CU_TENSOR_MAP_DATA_TYPE_INT32, q, 2, qd, qs, qb, qswz)) return false;
     const uint64_t sd[2] = {static_cast<uint64_t>(N), E * groups};
     const uint64_t ss[1] = {static_cast<uint64_t>(N) * 2};
     const uint32_t sb[2] = {kTileRows, sg};
@@ -203,10 +215,10 @@ bool make_token_map(CUtensorMap* m, const void* base, int64_t K, int64_t rows, i
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, base, 2, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-cudaError_t launch_gemm(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t st,
+cudaError_t launch_gemm(int bits, int act, int scl, int gemm, int lean, dim3 grid, size_t smem, cudaStream_t st,
                         const GemmMaps& m, const GemmArgs& a) {
-  return bits == 4 ? launch_gemm_w4(act, scl, gemm, grid, smem, st, m.q, m.s, m.z, m.b, a)
-                   : launch_gemm_w8(act, scl, gemm, grid, smem, st, m.q, m.s, m.z, m.b, a);
+  return bits == 4 ? launch_gemm_w4(act, scl, gemm, lean, grid, smem, st, m.q, m.s, m.z, m.b, a)
+                   : launch_gemm_w8(act, scl, gemm, lean, grid, smem, st, m.q, m.s, m.z, m.b, a);
 }
 
 struct Resolved {
@@ -343,8 +355,8 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   if (!mark(0) || launch_align(topk_ids, P, E, B, static_cast<int>(cap), sorted, experts, npp, counts, status,
                                slot_of_pair, s) != cudaSuccess)
     return WNA16_ERR_CUDA;
-  if (!mark(1) || launch_gather(hidden, topk_ids, slot_of_pair, P, topk, E, static_cast<int>(H), sm_count() * 8,
-                                x_sorted, s) != cudaSuccess)
+  if (!mark(1) || launch_gather(hidden, topk_ids, slot_of_pair, P, topk, E, static_cast<int>(H), bits == 4 ? 1 : 0,
+                                sm_count() * 8, x_sorted, s) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
   const Pipe pipe = pipe_for(bits, B);
@@ -378,7 +390,7 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles;
   const int64_t slots = static_cast<int64_t>(sms) * pipe.ctas_per_sm;
   const dim3 grid1(static_cast<unsigned>(std::min<int64_t>(units1, slots)));
-  if (!mark(2) || launch_gemm(bits, act_dtype, scale_dtype, 1, grid1, pipe.smem, s, m1, a1) != cudaSuccess)
+  if (!mark(2) || launch_gemm(bits, act_dtype, scale_dtype, 1, pipe.lean, grid1, pipe.smem, s, m1, a1) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
   GemmArgs a2 = a1;
@@ -393,7 +405,7 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a2.split = r.split;
   const int64_t units2 = static_cast<int64_t>(max_blocks) * a2.n_tiles * a2.split;
   const dim3 grid2(static_cast<unsigned>(std::min<int64_t>(units2, slots)));
-  if (!mark(3) || launch_gemm(bits, act_dtype, scale_dtype, 2, grid2, pipe.smem, s, m2, a2) != cudaSuccess)
+  if (!mark(3) || launch_gemm(bits, act_dtype, scale_dtype, 2, pipe.lean, grid2, pipe.smem, s, m2, a2) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
   if (!mark(4) || launch_combine(slab, topk_ids, static_cast<int>(M), static_cast<int>(H), topk, E, r.split,
