@@ -173,14 +173,6 @@ __device__ __forceinline__ int unit_expert(const GemmArgs& a, int blk) {
   return (e >= 0 && e < a.E) ? e : 0;  // blocks below num_post_pad always hold a valid id
 }
 
-// Warp-uniform bounded wait: lane 0 polls, the result is broadcast.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
-  int ok = 0;
-  if (lane_id() == 0) ok = wait_bar(bar, parity, abort_flag, status) ? 1 : 0;
-  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-}
-
 // Epilogue of one work unit, run by four warps covering the four TMEM lane
 // quarters: waits for the unit's accumulator, reads it 16 token columns at a
 // time and writes silu(gate) * up to the act cache (gate/up GEMM) or the
@@ -191,7 +183,7 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
                                               uint32_t acc_phase, uint64_t* accfull, uint64_t* accempty,
                                               volatile int* abort_flag, int q, int lane) {
   const int NT = a.block;
-  if (!warp_wait(&accfull[acc], acc_phase, abort_flag, a.status)) return false;
+  if (!warp_wait_all(&accfull[acc], acc_phase, abort_flag, a.status)) return false;
   tc_fence_after();
   const uint32_t t_base = tmem + ((q * 32) << 16) + acc * NT;
   for (int c0 = 0; c0 < NT; c0 += 16) {
@@ -317,18 +309,20 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     // Per stage: codes of 128 rows (gate/up: one 3D box holding the 64 gate and
     // the 64 up rows), their scales and zero points (one box each), and the two
     // 64-wide K chunks of the token tile: five copies for 8-16 KB of codes.
-    if (lane == 0) {
-      const uint32_t stage_tx = W_BYTES + SG * 256 + (a.has_zeros ? SG * (kTileRows / PF) * 4 : 0) + BST;
-      const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
-      const uint64_t pol_b = l2_policy_evict_last();   // token rows: re-read by every row tile
-      int it = 0, s = 0;
-      uint32_t e_phase = 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const Unit w = decode_unit(u, nb, a);
-        const int e = unit_expert(a, w.blk);
-        bool ok = true;
-        for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
-          if (!wait_bar(&empty[s], e_phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
+    // The whole warp runs the loop (waits are warp-wide polls); one elected
+    // lane issues the copies.
+    const uint32_t stage_tx = W_BYTES + SG * 256 + (a.has_zeros ? SG * (kTileRows / PF) * 4 : 0) + BST;
+    const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+    const uint64_t pol_b = l2_policy_evict_last();   // token rows: re-read by every row tile
+    int it = 0, s = 0;
+    uint32_t e_phase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit w = decode_unit(u, nb, a);
+      const int e = unit_expert(a, w.blk);
+      bool ok = true;
+      for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
+        if (!warp_wait_all(&empty[s], e_phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
+        if (elect_one()) {
           mbar_arrive_expect_tx(&full[s], stage_tx);
           uint8_t* dst = wring + s * WST;
           const int ys = e * a.groups + (kt * kTileK) / a.G;
@@ -348,39 +342,40 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
           for (int c = 0; c < kTileK / kChunkK; ++c)
             tma_load_2d(bring + s * BST + c * NT * 128, &tm_b, &full[s], kt * kTileK + c * kChunkK, w.blk * NT,
                         pol_b);
-          if (++s == NS) {
-            s = 0;
-            e_phase ^= 1u;
-          }
         }
-        if (!ok) break;
+        __syncwarp();
+        if (++s == NS) {
+          s = 0;
+          e_phase ^= 1u;
+        }
       }
-      // Let every issued copy land before the CTA can exit.
-      for (int j = (it > NS ? it - NS : 0); j < it; ++j) wait_bar_drain(&full[j % NS], (j / NS) & 1);
+      if (!ok) break;
     }
+    // Let every issued copy land before the CTA can exit.
+    for (int j = (it > NS ? it - NS : 0); j < it; ++j) wait_bar_drain(&full[j % NS], (j / NS) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Kept lean (wrapping counters, precomputed descriptors, unrolled MMAs):
-    // this single thread issues every MMA of the CTA and shares its SM
-    // sub-partition with dequant warps.
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16(ACT, NT);
-      const uint32_t a_base = tmem + NACC * NT;
-      const uint64_t chunk_step = static_cast<uint64_t>((NT * 128) >> 4);  // next 64-wide K chunk
-      int s = 0, slot = 0, uc = 0;
-      uint32_t a_phase = 0;
-      bool issued = false;
-      for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
-        const Unit w = decode_unit(u, nb, a);
-        const int acc = uc % NACC;
-        if (!wait_bar(&accempty[acc], ((uc / NACC) & 1) ^ 1, abort_flag, a.status)) break;
+    // The whole warp runs the loop and one elected lane issues: with the loop
+    // values warp-uniform, an 8-MMA stage issues several times faster than from
+    // a lone lane. Wrapping counters, precomputed descriptors, unrolled MMAs.
+    const uint32_t idesc = idesc_f16(ACT, NT);
+    const uint32_t a_base = tmem + NACC * NT;
+    const uint64_t chunk_step = static_cast<uint64_t>((NT * 128) >> 4);  // next 64-wide K chunk
+    int s = 0, slot = 0, uc = 0;
+    uint32_t a_phase = 0;
+    bool issued = false;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
+      const Unit w = decode_unit(u, nb, a);
+      const int acc = uc % NACC;
+      if (!warp_wait_all(&accempty[acc], ((uc / NACC) & 1) ^ 1, abort_flag, a.status)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + acc * NT;
+      bool ok = true;
+      for (int kt = w.kt0; kt < w.kt1; ++kt) {
+        // afull implies the stage landed (the dequant warps waited on full[s])
+        if (!warp_wait_all(&afull[slot], a_phase, abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * NT;
-        bool ok = true;
-        for (int kt = w.kt0; kt < w.kt1; ++kt) {
-          // afull implies the stage landed (the dequant warps waited on full[s])
-          if (!wait_bar(&afull[slot], a_phase, abort_flag, a.status)) { ok = false; break; }
-          tc_fence_after();
+        if (elect_one()) {
           const uint32_t at = a_base + slot * kASlotCols;
           const uint64_t b0 = smem_desc_sw128(smem_u32(bring + s * BST));
           const uint64_t b1 = b0 + chunk_step;
@@ -393,20 +388,23 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
           mma_ts_acc(d_tmem, at + 48, b1 + 4, idesc);
           mma_ts_acc(d_tmem, at + 56, b1 + 6, idesc);
           mma_commit(&empty[s]);
-          issued = true;
-          if (++s == NS) s = 0;
-          if (++slot == NA) {
-            slot = 0;
-            a_phase ^= 1u;
-          }
         }
-        if (!ok) break;
-        mma_commit(&accfull[acc]);
+        __syncwarp();
+        issued = true;
+        if (++s == NS) s = 0;
+        if (++slot == NA) {
+          slot = 0;
+          a_phase ^= 1u;
+        }
       }
-      if (issued) {
-        mma_commit(drain);
-        wait_bar_drain(drain, 0);
-      }
+      if (!ok) break;
+      if (elect_one()) mma_commit(&accfull[acc]);
+      __syncwarp();
+    }
+    if (issued) {
+      if (elect_one()) mma_commit(drain);
+      __syncwarp();
+      wait_bar_drain(drain, 0);
     }
   } else if (!LEAN && warp < 2 + kEpilogueWarps) {
     // ------------------------------------------------------------ epilogue
@@ -462,9 +460,9 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
           p_phase ^= 1u;
         }
         if (!LEAN && (it & 1) != grp) continue;
-        if (!warp_wait(&full[cs], cf, abort_flag, a.status)) { ok = false; break; }
+        if (!warp_wait_all(&full[cs], cf, abort_flag, a.status)) { ok = false; break; }
         if (it >= NA) {
-          if (!warp_wait(&empty[cps], cp, abort_flag, a.status)) { ok = false; break; }
+          if (!warp_wait_all(&empty[cps], cp, abort_flag, a.status)) { ok = false; break; }
         }
         const uint8_t* st = wring + cs * WST;
         // scale and zero point of each 64-wide chunk of the stage (group rows 0/1 when G = 64)

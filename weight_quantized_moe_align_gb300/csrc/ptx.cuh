@@ -88,6 +88,28 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
+// wait_bar for a whole converged warp. Every lane polls the same barrier in the
+// same instructions; the vote keeps the warp converged and the result uniform,
+// so the caller can go on with warp-uniform code (elect_one below).
+__device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              int* status) {
+  return __all_sync(0xFFFFFFFFu, wait_bar(bar, parity, abort_flag, status));
+}
+
+// One lane of a converged warp (the lowest) is elected. Issuing tcgen05.mma and
+// TMA copies from inside an elect block of a converged warp keeps their
+// operands warp-uniform; the same loop run by lane 0 alone issues several
+// times slower.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Same bound, ignoring the abort flag: used to drain copies before exit.
 __device__ __forceinline__ bool wait_bar_drain(uint64_t* bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer();
