@@ -87,6 +87,39 @@ def test_formats(act, sdt, bits, zeros, G):
     check(li, block=64)
 
 
+@pytest.mark.parametrize("act,sdt,bits,zeros", [("f16", "f16", 4, True), ("f16", "bf16", 4, False),
+                                                ("bf16", "bf16", 4, True), ("bf16", "f16", 4, False),
+                                                ("f16", "f16", 8, True), ("f16", "bf16", 8, False)])
+@pytest.mark.parametrize("G", [128, 256, -1])
+def test_deferred_scale_tiles(act, sdt, bits, zeros, G):
+    # 16-token tiles whose K stages lie inside one group run the deferred-scale
+    # kernel: magic-number codes, offsets and zero point removed by a correction
+    # MMA, scale applied to each stage's fp32 partial sum
+    wl = small(bits=bits, has_zeros=zeros, group_size=G, act_dtype=act, scale_dtype=sdt, H=512, I=768)
+    li = make_layer_inputs(wl, 37).to(DEV)
+    for split in (1, 2, 3):
+        check(li, block=16, split_k=split)
+
+
+@pytest.mark.parametrize("bits,act", [(4, "f16"), (4, "bf16"), (8, "f16")])
+def test_deferred_scale_half_stage(bits, act):
+    # per-channel scales, H and I = 64 (mod 128): the last K stage of both GEMMs
+    # holds a single 64-wide half, whose token sums stay zero
+    wl = small(H=320, I=192, group_size=-1, bits=bits, has_zeros=True, act_dtype=act, scale_dtype=act)
+    li = make_layer_inputs(wl, 23).to(DEV)
+    check(li, block=16)
+    check(li, block=16, split_k=2)
+
+
+def test_deferred_scale_large_activations():
+    # hidden values 50x larger: the fp16 token sums of the correction operand
+    # (stored at 1/32) and the magic-number offsets must not lose the result
+    wl = small(H=512, I=256, group_size=128)
+    li = make_layer_inputs(wl, 16).to(DEV)
+    li.hidden.mul_(50.0)
+    check(li, block=16)
+
+
 def test_hidden_not_multiple_of_row_tile():
     # H = 320: the down GEMM's last 128-row tile is half outside the matrix
     li = make_layer_inputs(small(H=320, I=128, group_size=64), 11).to(DEV)

@@ -19,6 +19,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace wna16 {
@@ -153,31 +155,69 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
 }
 
 // Copies the hidden row of every routed pair to its expert-sorted slot:
-// x_sorted[slot_of_pair[p]] = hidden[p / topk] (16-byte vectors of 8 elements).
-// With `permute` (int4 weights) each vector is stored in the GEMM's K order
-// 0,4,1,5,2,6,3,7. Padded slots are not written: they only feed MMA columns
-// whose results are discarded.
+// x_sorted[slot_of_pair[p]] = hidden[p / topk], one thread per 64-element
+// chunk (eight 16-byte vectors). With `permute` (int4 weights) each vector is
+// stored in the GEMM's K order 0,4,1,5,2,6,3,7. With `xs` the thread also
+// writes the fp32 sums of the chunk's even-k and odd-k values, the token sums
+// of the deferred-scale gate/up GEMM: xs[(stage * 4 + 2 * half + parity) * cap
+// + slot], stage = chunk / 2, half = chunk % 2. Padded slots are not written:
+// they only feed MMA columns whose results are discarded.
+template <int ACT>
+__device__ __forceinline__ void add_even_odd(uint32_t w, float& se, float& so) {
+  if constexpr (ACT == 0) {
+    se += __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+    so += __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+  } else {
+    se += __uint_as_float(w << 16);
+    so += __uint_as_float(w & 0xFFFF0000u);
+  }
+}
+
+template <int ACT>
 __global__ void __launch_bounds__(256)
     moe_gather_kernel(const uint4* __restrict__ hidden, const int32_t* __restrict__ ids,
                       const int32_t* __restrict__ slot_of_pair, int P, int topk, int E, int h8, int permute,
-                      uint4* __restrict__ x_sorted) {
-  const long long n = static_cast<long long>(P) * h8;
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int p = static_cast<int>(idx / h8);
-    const int c = static_cast<int>(idx % h8);
+                      uint4* __restrict__ x_sorted, float* __restrict__ xs, int cap, float* __restrict__ zero0,
+                      int zero_n0, float* __restrict__ zero1, int zero_n1) {
+  const int chunks = h8 / 8;
+  const long long n = static_cast<long long>(P) * chunks;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long first = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (long long idx = first; idx < n; idx += stride) {
+    const int p = static_cast<int>(idx / chunks);
+    const int c = static_cast<int>(idx % chunks);
     const int e = ids[p];
     if (e < 0 || e >= E) continue;
-    uint4 v = hidden[static_cast<long long>(p / topk) * h8 + c];
-    if (permute) {  // (x0 x1)(x2 x3)(x4 x5)(x6 x7) -> (x0 x4)(x1 x5)(x2 x6)(x3 x7)
-      const uint4 u = v;
-      v.x = __byte_perm(u.x, u.z, 0x5410);
-      v.y = __byte_perm(u.x, u.z, 0x7632);
-      v.z = __byte_perm(u.y, u.w, 0x5410);
-      v.w = __byte_perm(u.y, u.w, 0x7632);
+    const int slot = slot_of_pair[p];
+    const uint4* src = hidden + static_cast<long long>(p / topk) * h8 + c * 8;
+    uint4* dst = x_sorted + static_cast<long long>(slot) * h8 + c * 8;
+    float se = 0.f, so = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint4 v = src[i];
+      if (xs) {
+        add_even_odd<ACT>(v.x, se, so);
+        add_even_odd<ACT>(v.y, se, so);
+        add_even_odd<ACT>(v.z, se, so);
+        add_even_odd<ACT>(v.w, se, so);
+      }
+      if (permute) {  // (x0 x1)(x2 x3)(x4 x5)(x6 x7) -> (x0 x4)(x1 x5)(x2 x6)(x3 x7)
+        const uint4 u = v;
+        v.x = __byte_perm(u.x, u.z, 0x5410);
+        v.y = __byte_perm(u.x, u.z, 0x7632);
+        v.z = __byte_perm(u.y, u.w, 0x5410);
+        v.w = __byte_perm(u.y, u.w, 0x7632);
+      }
+      dst[i] = v;
     }
-    x_sorted[static_cast<long long>(slot_of_pair[p]) * h8 + c] = v;
+    if (xs) {
+      const long long base = (static_cast<long long>(c >> 1) * 4 + (c & 1) * 2) * cap + slot;
+      xs[base] = se;
+      xs[base + cap] = so;
+    }
   }
+  for (long long i = first; i < zero_n0; i += stride) zero0[i] = 0.f;
+  for (long long i = first; i < zero_n1; i += stride) zero1[i] = 0.f;
 }
 
 template <typename T>
@@ -225,15 +265,24 @@ cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, i
 }
 
 cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
-                          int topk, int E, int H, int permute, int max_ctas, void* x_sorted, cudaStream_t stream) {
+                          int topk, int E, int H, int permute, int act_dtype, int max_ctas, void* x_sorted,
+                          float* xs, int cap, float* zero_ptr0, int zero_n0, float* zero_ptr1, int zero_n1,
+                          cudaStream_t stream) {
   const int h8 = H / 8;
-  const long long n = static_cast<long long>(P) * h8;
+  long long n = static_cast<long long>(P) * (h8 / 8);
+  n = std::max<long long>(n, std::max(zero_n0, zero_n1));
   const int threads = 256;
   const long long want = (n + threads - 1) / threads;
   const unsigned blocks = static_cast<unsigned>(want < max_ctas ? want : max_ctas);
   if (blocks == 0) return cudaSuccess;
-  moe_gather_kernel<<<blocks, threads, 0, stream>>>(static_cast<const uint4*>(hidden), ids, slot_of_pair, P,
-                                                    topk, E, h8, permute, static_cast<uint4*>(x_sorted));
+  if (act_dtype == 0)
+    moe_gather_kernel<0><<<blocks, threads, 0, stream>>>(static_cast<const uint4*>(hidden), ids, slot_of_pair, P,
+                                                         topk, E, h8, permute, static_cast<uint4*>(x_sorted), xs,
+                                                         cap, zero_ptr0, zero_n0, zero_ptr1, zero_n1);
+  else
+    moe_gather_kernel<1><<<blocks, threads, 0, stream>>>(static_cast<const uint4*>(hidden), ids, slot_of_pair, P,
+                                                         topk, E, h8, permute, static_cast<uint4*>(x_sorted), xs,
+                                                         cap, zero_ptr0, zero_n0, zero_ptr1, zero_n1);
   return cudaGetLastError();
 }
 

@@ -65,6 +65,8 @@ struct GemmArgs {
   int num_aslots;
   int num_acc;
   uint32_t tmem_cols;
+  float* xs_out;               // deferred-scale gate/up GEMM: token sums of the act cache per down stage
+  int cap;                     // rows of the expert-sorted token matrices
 };
 
 // One weight stage in shared memory: packed codes of 128 rows x 128 K, then up
@@ -83,6 +85,16 @@ __host__ __device__ constexpr int gemm_extra_bytes() { return 8 * (2 * kMaxStage
 __host__ __device__ constexpr int gemm_smem_bytes(int bits, int block, int stages) {
   return 1024 /* base alignment slack */ + weight_ring_bytes(bits, stages) + stages * token_stage_bytes(block) +
          gemm_extra_bytes();
+}
+
+// Deferred-scale kernel (16-token tiles): ring stages of weights, tokens and
+// per-stage token sums (4 parts x 16 floats for the gate/up GEMM, 16 parts for
+// the down GEMM), two correction-operand tiles (16 rows of 128 B) and barriers.
+constexpr int kDeferNT = 16;
+__host__ __device__ constexpr int defer_xs_parts(int gemm) { return gemm == 1 ? 4 : 16; }
+__host__ __device__ constexpr int defer_smem_bytes(int bits, int gemm, int stages) {
+  return 1024 + weight_ring_bytes(bits, stages) + stages * token_stage_bytes(kDeferNT) + 2 * kDeferNT * 128 +
+         stages * defer_xs_parts(gemm) * kDeferNT * 4 + 8 * (2 * stages + 8) + 64;
 }
 
 }  // namespace wna16

@@ -13,11 +13,21 @@ cudaError_t launch_gemm_w8(int act, int scl, int gemm, int lean, dim3 grid, size
                            const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                            const CUtensorMap& b, const GemmArgs& a);
 
+// Deferred-scale GEMM for 16-token tiles; `x` maps the per-stage token sums.
+bool defer_supported(int bits, int act);
+cudaError_t launch_gemm_defer(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
+                              const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
+                              const CUtensorMap& b, const CUtensorMap& x, const GemmArgs& a);
+
 cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* num_post_pad, int32_t* counts,
                          int32_t* status, int32_t* slot_of_pair, cudaStream_t stream);
+// Expert-sorted copy of the hidden rows; with `xs` also the deferred-scale
+// token sums [H/128 stages][4 parts][cap] and zeros for the `zero_n` floats at
+// each `zero_ptr` (token-sum parts of a stage half with no K elements).
 cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
-                          int topk, int E, int H, int permute, int max_ctas, void* x_sorted,
+                          int topk, int E, int H, int permute, int act_dtype, int max_ctas, void* x_sorted,
+                          float* xs, int cap, float* zero_ptr0, int zero_n0, float* zero_ptr1, int zero_n1,
                           cudaStream_t stream);
 cudaError_t launch_combine(const float* slab, const int32_t* ids, int M, int H, int topk, int E,
                            int split, int act_dtype, void* out, cudaStream_t stream);

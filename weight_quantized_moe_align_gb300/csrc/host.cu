@@ -83,6 +83,13 @@ Pipe pipe_for(int bits, int block) {
   return p;
 }
 
+// Stages of the deferred-scale kernel (two CTAs per SM).
+int defer_stages(int bits, int gemm) {
+  int st = kMaxStages;
+  while (st > 2 && defer_smem_bytes(bits, gemm, st) > kHalfSmem) --st;
+  return st;
+}
+
 int choose_split(int64_t units, int kt_total, int ctas_per_sm) {
   const int slots = sm_count() * ctas_per_sm;
   if (units >= slots) return 1;
@@ -93,7 +100,7 @@ int choose_split(int64_t units, int kt_total, int ctas_per_sm) {
 }
 
 struct WsLayout {
-  size_t status, sorted, experts, npp, counts, slot_of_pair, x_sorted, act, slab, total;
+  size_t status, sorted, experts, npp, counts, slot_of_pair, x_sorted, act, slab, xs1, xs2, total;
 };
 
 WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, int split) {
@@ -115,6 +122,13 @@ WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, 
   w.x_sorted = take(static_cast<size_t>(cap) * H * 2);
   w.act = take(static_cast<size_t>(cap) * I * 2);
   w.slab = take(static_cast<size_t>(split) * P * H * 4);
+  // token sums of the deferred-scale GEMMs (16-token tiles only):
+  // [H/128 stages][4][cap] and [I/128 stages][16][cap] floats
+  const size_t kt1 = static_cast<size_t>((H + kTileK - 1) / kTileK);
+  const size_t kt2 = static_cast<size_t>((I + kTileK - 1) / kTileK);
+  const bool defer = block == kDeferNT;
+  w.xs1 = take(defer ? kt1 * defer_xs_parts(1) * cap * 4 : 0);
+  w.xs2 = take(defer ? kt2 * defer_xs_parts(2) * cap * 4 : 0);
   w.total = o;
   return w;
 }
@@ -213,6 +227,15 @@ bool make_token_map(CUtensorMap* m, const void* base, int64_t K, int64_t rows, i
   const uint64_t st[1] = {static_cast<uint64_t>(K) * 2};
   const uint32_t b[2] = {kChunkK, static_cast<uint32_t>(block)};
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, base, 2, d, st, b, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Token sums of a deferred-scale GEMM: fp32 [stages][parts][rows], box
+// {16 rows, parts, 1 stage}.
+bool make_xs_map(CUtensorMap* m, const float* base, int64_t rows, int parts, int stages) {
+  const uint64_t d[3] = {static_cast<uint64_t>(rows), static_cast<uint64_t>(parts), static_cast<uint64_t>(stages)};
+  const uint64_t st[2] = {static_cast<uint64_t>(rows) * 4, static_cast<uint64_t>(rows) * parts * 4};
+  const uint32_t b[3] = {static_cast<uint32_t>(kDeferNT), static_cast<uint32_t>(parts), 1};
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, 3, d, st, b);
 }
 
 cudaError_t launch_gemm(int bits, int act, int scl, int gemm, int lean, dim3 grid, size_t smem, cudaStream_t st,
@@ -338,6 +361,13 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   const int64_t cap = capacity(P, E, B);
   const int max_blocks = static_cast<int>(cap / B);
   const bool zeros = w13_zeros != nullptr;
+  // 16-token tiles run the deferred-scale kernel when every stage lies in one
+  // group (G >= 128) and the code/activation formats have a magic-number form.
+  const bool defer = B == kDeferNT && r.G1 >= kTileK && r.G2 >= kTileK && defer_supported(bits, act_dtype);
+  const int kt1 = static_cast<int>((H + kTileK - 1) / kTileK);
+  const int kt2 = static_cast<int>((I + kTileK - 1) / kTileK);
+  float* xs1 = defer ? reinterpret_cast<float*>(ws + L.xs1) : nullptr;
+  float* xs2 = defer ? reinterpret_cast<float*>(ws + L.xs2) : nullptr;
 
   auto mark = [&](int i) {
     if (events && events[i]) return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
@@ -351,12 +381,29 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   // 128-byte swizzled K-major layout (gathered hidden rows; the act cache).
   if (!make_token_map(&m1.b, x_sorted, H, cap, B) || !make_token_map(&m2.b, act, I, cap, B))
     return WNA16_ERR_CUDA;
+  CUtensorMap x1{}, x2{};
+  if (defer && (!make_xs_map(&x1, xs1, cap, defer_xs_parts(1), kt1) ||
+                !make_xs_map(&x2, xs2, cap, defer_xs_parts(2), kt2)))
+    return WNA16_ERR_CUDA;
 
   if (!mark(0) || launch_align(topk_ids, P, E, B, static_cast<int>(cap), sorted, experts, npp, counts, status,
                                slot_of_pair, s) != cudaSuccess)
     return WNA16_ERR_CUDA;
+  // Token-sum parts of a stage half that holds no K elements stay zero.
+  float* zero1 = nullptr;
+  float* zero2 = nullptr;
+  int zero1_n = 0, zero2_n = 0;
+  if (defer && H % kTileK) {
+    zero1 = xs1 + (static_cast<size_t>(kt1 - 1) * 4 + 2) * cap;
+    zero1_n = static_cast<int>(2 * cap);
+  }
+  if (defer && I % kTileK) {
+    zero2 = xs2 + (static_cast<size_t>(kt2 - 1) * 16 + 8) * cap;
+    zero2_n = static_cast<int>(8 * cap);
+  }
   if (!mark(1) || launch_gather(hidden, topk_ids, slot_of_pair, P, topk, E, static_cast<int>(H), bits == 4 ? 1 : 0,
-                                sm_count() * 8, x_sorted, s) != cudaSuccess)
+                                act_dtype, sm_count() * 8, x_sorted, xs1, static_cast<int>(cap), zero1, zero1_n,
+                                zero2, zero2_n, s) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
   const Pipe pipe = pipe_for(bits, B);
@@ -387,11 +434,21 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a1.num_aslots = pipe.aslots;
   a1.num_acc = pipe.acc;
   a1.tmem_cols = pipe.tmem_cols;
+  a1.xs_out = xs2;
+  a1.cap = static_cast<int>(cap);
   const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles;
   const int64_t slots = static_cast<int64_t>(sms) * pipe.ctas_per_sm;
   const dim3 grid1(static_cast<unsigned>(std::min<int64_t>(units1, slots)));
-  if (!mark(2) || launch_gemm(bits, act_dtype, scale_dtype, 1, pipe.lean, grid1, pipe.smem, s, m1, a1) != cudaSuccess)
-    return WNA16_ERR_CUDA;
+  if (!mark(2)) return WNA16_ERR_CUDA;
+  cudaError_t e1;
+  if (defer) {
+    a1.num_stages = defer_stages(bits, 1);
+    e1 = launch_gemm_defer(bits, act_dtype, scale_dtype, 1, grid1, defer_smem_bytes(bits, 1, a1.num_stages), s,
+                           m1.q, m1.s, m1.z, m1.b, x1, a1);
+  } else {
+    e1 = launch_gemm(bits, act_dtype, scale_dtype, 1, pipe.lean, grid1, pipe.smem, s, m1, a1);
+  }
+  if (e1 != cudaSuccess) return WNA16_ERR_CUDA;
 
   GemmArgs a2 = a1;
   a2.out = slab;
@@ -405,8 +462,16 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a2.split = r.split;
   const int64_t units2 = static_cast<int64_t>(max_blocks) * a2.n_tiles * a2.split;
   const dim3 grid2(static_cast<unsigned>(std::min<int64_t>(units2, slots)));
-  if (!mark(3) || launch_gemm(bits, act_dtype, scale_dtype, 2, pipe.lean, grid2, pipe.smem, s, m2, a2) != cudaSuccess)
-    return WNA16_ERR_CUDA;
+  if (!mark(3)) return WNA16_ERR_CUDA;
+  cudaError_t e2;
+  if (defer) {
+    a2.num_stages = defer_stages(bits, 2);
+    e2 = launch_gemm_defer(bits, act_dtype, scale_dtype, 2, grid2, defer_smem_bytes(bits, 2, a2.num_stages), s,
+                           m2.q, m2.s, m2.z, m2.b, x2, a2);
+  } else {
+    e2 = launch_gemm(bits, act_dtype, scale_dtype, 2, pipe.lean, grid2, pipe.smem, s, m2, a2);
+  }
+  if (e2 != cudaSuccess) return WNA16_ERR_CUDA;
 
   if (!mark(4) || launch_combine(slab, topk_ids, static_cast<int>(M), static_cast<int>(H), topk, E, r.split,
                                  act_dtype, out, s) != cudaSuccess)
