@@ -101,25 +101,25 @@ __device__ __forceinline__ uint32_t pack_b2(__nv_bfloat16 lo, __nv_bfloat16 hi) 
 // one sum with the single offset in positions 0..2.
 template <int BITS, int ACT>
 __device__ __forceinline__ void corr_a(uint32_t zero, uint32_t (&c)[8]) {
+  // The values are built from their bit patterns: for c = 2^e (1 + m) the
+  // scaled copies differ only in the exponent field (z < 2^10 for offset 1024,
+  // z < 2^6 for offset 64, z < 2^7 for the bf16 offset 128).
   if constexpr (ACT == 0) {
-    const float ce = 1024.f + float(zero);  // even k (all k for int8)
-    const float co = 64.f + float(zero);                           // odd k (int4)
-    const __half e1 = __float2half_rn(-32.f * ce), e2 = __float2half_rn(-ce * (1.f / 64.f)),
-                 e3 = __float2half_rn(-ce * (1.f / 131072.f));
+    // even k: -32 (1024 + z) = 0xF800 | z, -(1024 + z) / 64 = 0xCC00 | z,
+    //         -(1024 + z) 2^-17 = 0xA000 | z
+    c[0] = 0xCC00F800u | (zero * 0x10001u);
     if constexpr (BITS == 4) {
-      const __half o1 = __float2half_rn(-32.f * co), o2 = __float2half_rn(-co * (1.f / 64.f)),
-                   o3 = __float2half_rn(-co * (1.f / 131072.f));
-      c[0] = pack_h2(e1, e2);
-      c[1] = pack_h2(e3, o1);
-      c[2] = pack_h2(o2, o3);
+      // odd k: -32 (64 + z) = 0xE800 | z << 4, -(64 + z) / 64 = 0xBC00 | z << 4,
+      //        -(64 + z) 2^-17 = 0x9000 | z << 4
+      c[1] = 0xE800A000u | (zero << 20) | zero;
+      c[2] = 0x9000BC00u | ((zero << 4) * 0x10001u);
     } else {
-      c[0] = pack_h2(e1, e2);
-      c[1] = pack_h2(e3, __float2half_rn(0.f));
+      c[1] = 0x0000A000u | zero;
     }
   } else {
-    const __nv_bfloat16 v = __float2bfloat16_rn(-(128.f + float(zero)));
-    c[0] = pack_b2(v, v);
-    c[1] = pack_b2(v, __float2bfloat16_rn(0.f));
+    const uint32_t v = 0xC300u | zero;  // -(128 + z) in bf16
+    c[0] = v * 0x10001u;
+    c[1] = v;
   }
 }
 
@@ -351,22 +351,19 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     const uint4* row_base = reinterpret_cast<const uint4*>(wring + srow * KW * 4);
     const int swz = BITS == 4 ? ((srow >> 1) & 3) : (srow & 7);
 
-    int it = 0, s = 0, uc = 0;
-    uint32_t f_phase = 0;
+    // This group's stages are the running stage indices g, g + 2, g + 4, ...
+    // across units: ring slot cs and phase cf of the next one advance by two
+    // slots, the afull / pfull phase pph flips each time.
+    int it = 0, uc = 0, cs = g;
+    uint32_t cf = 0, pph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
       const Unit w = decode_unit(u, nb, a);
+      const int n = w.kt1 - w.kt0;
       float acc[NT];
 #pragma unroll
       for (int j = 0; j < NT; ++j) acc[j] = 0.f;
-      for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
-        const int cs = s;
-        const uint32_t cf = f_phase;
-        if (++s == NS) {
-          s = 0;
-          f_phase ^= 1u;
-        }
-        if ((it & 1) != g) continue;
+      for (int i = (g - it) & 1; i < n; i += 2) {
         if (!warp_wait_all(&full[cs], cf, abort_flag, a.status)) { ok = false; break; }
         const uint8_t* st = wring + cs * WST;
         const float scale = scale_to_f32<SCL>(reinterpret_cast<const uint16_t*>(st + S_OFF)[si]);
@@ -416,14 +413,21 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[g]);
         // this stage's partial sum, scaled into the accumulators
-        if (!warp_wait_all(&pfull[g], (it >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+        if (!warp_wait_all(&pfull[g], pph, abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
         uint32_t v[16];
         tmem_ld16(p_addr, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < NT; ++j) acc[j] = fmaf(scale, __uint_as_float(v[j]), acc[j]);
+        pph ^= 1u;
+        cs += 2;
+        if (cs >= NS) {
+          cs -= NS;
+          cf ^= 1u;
+        }
       }
+      it += n;
       if (!ok) break;
       // combine the two warpgroups' sums (buffer C), epilogue in warpgroup 0
       if (g == 1) {
