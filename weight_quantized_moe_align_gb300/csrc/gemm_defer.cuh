@@ -247,16 +247,20 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     const uint64_t pol_b = l2_policy_evict_last();
     int it = 0, s = 0;
     uint32_t e_phase = 0;
+    // stages per quantization group: G is a multiple of 128, or the whole K
+    // (per-channel scales, one group), where rounding up keeps every stage in it
+    const int spg = (a.G + kTileK - 1) / kTileK;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = decode_unit(u, nb, a);
       const int e = unit_expert(a, w.blk);
+      // scale / zero-point row of the current stage, advanced per group
+      int ys = e * a.groups + w.kt0 / spg, gk = w.kt0 % spg;
       bool ok = true;
       for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
         if (!warp_wait_all(&empty[s], e_phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
         if (elect_one()) {
           mbar_arrive_expect_tx(&full[s], stage_tx);
           uint8_t* dst = wring + s * WST;
-          const int ys = e * a.groups + (kt * kTileK) / a.G;
           if (GEMM == 1) {
             const int f0 = w.tile * kGateUpRows;
             tma_load_3d(dst, &tm_q, &full[s], kt * KW, f0, 2 * e, pol_w);
@@ -278,6 +282,10 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         if (++s == NS) {
           s = 0;
           e_phase ^= 1u;
+        }
+        if (++gk == spg) {
+          gk = 0;
+          ++ys;
         }
       }
       if (!ok) break;

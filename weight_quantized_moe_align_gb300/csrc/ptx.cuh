@@ -89,10 +89,14 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 }
 
 // wait_bar for a whole converged warp. Every lane polls the same barrier in the
-// same instructions; the vote keeps the warp converged and the result uniform,
-// so the caller can go on with warp-uniform code (elect_one below).
+// same instructions; after a slow wait the vote keeps the warp converged and
+// the result uniform, so the caller can go on with warp-uniform code
+// (elect_one below).
 __device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               int* status) {
+  // The first probe is one warp-wide instruction reading one barrier word, so
+  // its result is the same in every lane; only the slow path needs the vote.
+  if (mbar_try_wait(bar, parity)) return true;
   return __all_sync(0xFFFFFFFFu, wait_bar(bar, parity, abort_flag, status));
 }
 
