@@ -42,7 +42,7 @@ from synthetic.workloads import make_routing  # noqa: E402
 METRIC = "fused W4A16 MoE layer tokens/s and achieved HBM GB/s (% of peak) vs batch M"
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
-KERNEL_SOURCES = ("gemm_kernel.cuh", "common.cuh", "ptx.cuh", "host.cu")
+KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_defer.cuh", "common.cuh", "ptx.cuh", "host.cu")
 
 
 def parse():
@@ -255,6 +255,18 @@ def host_cores():
 # arms
 # ----------------------------------------------------------------------------
 
+def gemm_kernel_name(w, wl, M, gemm):
+    """Name of the GEMM kernel the library launches for this workload (the
+    library's selection rule: 16-token tiles with every 128-wide K stage inside
+    one quantization group, and 4-bit codes or fp16 activations, run the
+    deferred-scale kernel)."""
+    block = w.choose_block(M, wl.topk, wl.E)
+    g = wl.group_size
+    defer = block == 16 and (g == -1 or g >= 128) and (wl.bits == 4 or wl.act_dtype == "f16")
+    base = "moe_gemm_defer_kernel" if defer else "moe_gemm_kernel"
+    return f"{base}<{wl.bits},{wl.act_dtype},{wl.scale_dtype},{gemm}>"
+
+
 def workload_label(wl, M):
     q = f"int{wl.bits} {'asym' if wl.has_zeros else 'sym'} g{wl.group_size if wl.group_size > 0 else 'channel'}"
     return (f"{wl.name}: H={wl.H} I={wl.I} E={wl.E} top{wl.topk} {wl.routing}, {q}, "
@@ -400,7 +412,7 @@ def ours_arm(args):
         achieved = dom[3] / (dom[1] / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"]}
-    kname = f"moe_gemm_kernel<{wl.bits},{wl.act_dtype},{wl.scale_dtype},{1 if dom[0] == 'gate_up_gemm' else 2}>"
+    kname = gemm_kernel_name(w, wl, M, 1 if dom[0] == "gate_up_gemm" else 2)
     roof.update({"traffic": ncu_traffic(f"{wl.name}/M={M}", kname), "kernel": dom[0],
                  "kernel_ms": dom[1], "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
                  if peaks["source"] == "measured" else "fallback",

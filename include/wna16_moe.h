@@ -30,8 +30,9 @@
  *   zeros  [E, K/G, N/pf] int32 zero point of row n in bits [bits*(n%pf), +bits)
  *                       of word n/pf; NULL = symmetric, zero point 2^(bits-1)
  *   with (N, K) = (2I, H) for w13 (rows [0,I) gate, [I,2I) up) and (H, I) for w2.
- *   group_size G: a multiple of 64 that divides K, or -1 for one group per
- *   output channel (G = K).
+ *   group_size G: 64 or a multiple of 128 that divides K (a 128-wide K stage
+ *   of the kernels never straddles two groups), or -1 for one group per output
+ *   channel (G = K).
  *
  * Ownership and threading. Every pointer is a non-owning DEVICE pointer on the
  * current CUDA device unless stated otherwise, 16-byte aligned. The library
@@ -127,7 +128,8 @@ size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, i
  *   w13_q/w13_scales/w13_zeros, w2_q/w2_scales/w2_zeros: layout above
  *                (zeros may be NULL; both NULL or both non-NULL).
  *   scale_dtype  dtype of both scale tensors.
- *   bits         4 or 8. group_size: multiple of 64 dividing H and I, or -1.
+ *   bits         4 or 8. group_size: 64 or a multiple of 128 dividing H and I,
+ *                or -1.
  *   topk_ids     [M, topk] int32; topk_weights [M, topk] fp32.
  *   out          [M, H] act_dtype, written (never read).
  *   workspace    device memory of at least wna16_fused_moe_workspace_bytes();
@@ -137,6 +139,13 @@ size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, i
  *   split_k      K-splits of the down GEMM (0 = automatic, else 1..8).
  * Shapes: H a multiple of 64, I a multiple of 64, 1 <= topk <= E <= 256,
  * M*topk < 2^31. M = 0 returns WNA16_OK and launches nothing.
+ * Numerics: fp32 accumulation, one rounding of the output; the act cache
+ * silu(g)*u is stored in act_dtype. Token tiles of 32+ rows dequantize each
+ * weight to act_dtype, (code - zero) * scale rounded once. 16-row tiles with
+ * G >= 128 or per-channel scales (int4, or int8 with fp16) never round the
+ * weights: the MMA multiplies exact integer codes and the zero point and scale
+ * are applied in fp32. With fp16 activations the sum of one 128-wide K
+ * stage's activations (of one token) must stay below about 2.1e6 there.
  */
 wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
                              int64_t I, int E, int topk, const int32_t* w13_q,
