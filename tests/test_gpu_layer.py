@@ -91,14 +91,15 @@ def test_formats(act, sdt, bits, zeros, G):
                                                 ("bf16", "bf16", 4, True), ("bf16", "f16", 4, False),
                                                 ("f16", "f16", 8, True), ("f16", "bf16", 8, False)])
 @pytest.mark.parametrize("G", [128, 256, -1])
-def test_deferred_scale_tiles(act, sdt, bits, zeros, G):
-    # 16-token tiles whose K stages lie inside one group run the deferred-scale
-    # kernel: magic-number codes, offsets and zero point removed by a correction
-    # MMA, scale applied to each stage's fp32 partial sum
+@pytest.mark.parametrize("block", [16, 32])
+def test_deferred_scale_tiles(act, sdt, bits, zeros, G, block):
+    # 16- and 32-token tiles whose K stages lie inside one group run the
+    # deferred-scale kernel: magic-number codes, offsets and zero point removed
+    # by a correction MMA, scale applied to each stage's fp32 partial sum
     wl = small(bits=bits, has_zeros=zeros, group_size=G, act_dtype=act, scale_dtype=sdt, H=512, I=768)
-    li = make_layer_inputs(wl, 37).to(DEV)
+    li = make_layer_inputs(wl, 37 if block == 16 else 75).to(DEV)
     for split in (1, 2, 3):
-        check(li, block=16, split_k=split)
+        check(li, block=block, split_k=split)
 
 
 @pytest.mark.parametrize("bits,act", [(4, "f16"), (4, "bf16"), (8, "f16")])
@@ -109,6 +110,7 @@ def test_deferred_scale_half_stage(bits, act):
     li = make_layer_inputs(wl, 23).to(DEV)
     check(li, block=16)
     check(li, block=16, split_k=2)
+    check(li, block=32, split_k=2)
 
 
 def test_deferred_scale_large_activations():
@@ -118,6 +120,7 @@ def test_deferred_scale_large_activations():
     li = make_layer_inputs(wl, 16).to(DEV)
     li.hidden.mul_(50.0)
     check(li, block=16)
+    check(li, block=32)
 
 
 def test_hidden_not_multiple_of_row_tile():

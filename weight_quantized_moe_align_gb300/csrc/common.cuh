@@ -87,14 +87,15 @@ __host__ __device__ constexpr int gemm_smem_bytes(int bits, int block, int stage
          gemm_extra_bytes();
 }
 
-// Deferred-scale kernel (16-token tiles): ring stages of weights, tokens and
-// per-stage token sums (4 parts x 16 floats for the gate/up GEMM, 16 parts for
-// the down GEMM), two correction-operand tiles (16 rows of 128 B) and barriers.
-constexpr int kDeferNT = 16;
+// Deferred-scale kernel (16- or 32-token tiles): ring stages of weights, tokens
+// and per-stage token sums (4 parts x nt floats for the gate/up GEMM, 16 parts
+// for the down GEMM), two correction-operand tiles (nt rows of 128 B) and
+// barriers.
+__host__ __device__ constexpr bool defer_tile(int block) { return block == 16 || block == 32; }
 __host__ __device__ constexpr int defer_xs_parts(int gemm) { return gemm == 1 ? 4 : 16; }
-__host__ __device__ constexpr int defer_smem_bytes(int bits, int gemm, int stages) {
-  return 1024 + weight_ring_bytes(bits, stages) + stages * token_stage_bytes(kDeferNT) + 2 * kDeferNT * 128 +
-         stages * defer_xs_parts(gemm) * kDeferNT * 4 + 8 * (2 * stages + 8) + 64;
+__host__ __device__ constexpr int defer_smem_bytes(int bits, int gemm, int nt, int stages) {
+  return 1024 + weight_ring_bytes(bits, stages) + stages * token_stage_bytes(nt) + 2 * nt * 128 +
+         stages * defer_xs_parts(gemm) * nt * 4 + 8 * (2 * stages + 8) + 64;
 }
 
 }  // namespace wna16

@@ -1,4 +1,4 @@
-// Instantiations of the deferred-scale grouped GEMM (16-token tiles).
+// Instantiations of the deferred-scale grouped GEMM (16- and 32-token tiles).
 #include "gemm_defer.cuh"
 #include "gemm_launch.cuh"
 
@@ -6,10 +6,10 @@ namespace wna16 {
 
 namespace {
 
-template <int BITS, int ACT, int SCL, int GEMM>
+template <int BITS, int ACT, int SCL, int GEMM, int NT>
 cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t stream, const CUtensorMap& q, const CUtensorMap& s,
                        const CUtensorMap& z, const CUtensorMap& b, const CUtensorMap& x, const GemmArgs& a) {
-  auto* fn = moe_gemm_defer_kernel<BITS, ACT, SCL, GEMM>;
+  auto* fn = moe_gemm_defer_kernel<BITS, ACT, SCL, GEMM, NT>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -23,20 +23,29 @@ cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t stream, const CUtens
   return cudaGetLastError();
 }
 
-template <int BITS, int GEMM>
+template <int BITS, int GEMM, int NT>
 cudaError_t by_dtype(int act, int scl, dim3 grid, size_t smem, cudaStream_t stream, const CUtensorMap& q,
                      const CUtensorMap& s, const CUtensorMap& z, const CUtensorMap& b, const CUtensorMap& x,
                      const GemmArgs& a) {
   if constexpr (BITS == 8) {
     if (act != 0) return cudaErrorInvalidValue;  // 8-bit codes: fp16 activations only
-    if (scl == 0) return launch_one<8, 0, 0, GEMM>(grid, smem, stream, q, s, z, b, x, a);
-    return launch_one<8, 0, 1, GEMM>(grid, smem, stream, q, s, z, b, x, a);
+    if (scl == 0) return launch_one<8, 0, 0, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
+    return launch_one<8, 0, 1, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
   } else {
-    if (act == 0 && scl == 0) return launch_one<4, 0, 0, GEMM>(grid, smem, stream, q, s, z, b, x, a);
-    if (act == 0 && scl == 1) return launch_one<4, 0, 1, GEMM>(grid, smem, stream, q, s, z, b, x, a);
-    if (act == 1 && scl == 0) return launch_one<4, 1, 0, GEMM>(grid, smem, stream, q, s, z, b, x, a);
-    return launch_one<4, 1, 1, GEMM>(grid, smem, stream, q, s, z, b, x, a);
+    if (act == 0 && scl == 0) return launch_one<4, 0, 0, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
+    if (act == 0 && scl == 1) return launch_one<4, 0, 1, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
+    if (act == 1 && scl == 0) return launch_one<4, 1, 0, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
+    return launch_one<4, 1, 1, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
   }
+}
+
+template <int BITS, int GEMM>
+cudaError_t by_tile(int nt, int act, int scl, dim3 grid, size_t smem, cudaStream_t stream, const CUtensorMap& q,
+                    const CUtensorMap& s, const CUtensorMap& z, const CUtensorMap& b, const CUtensorMap& x,
+                    const GemmArgs& a) {
+  if (nt == 16) return by_dtype<BITS, GEMM, 16>(act, scl, grid, smem, stream, q, s, z, b, x, a);
+  if (nt == 32) return by_dtype<BITS, GEMM, 32>(act, scl, grid, smem, stream, q, s, z, b, x, a);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -46,11 +55,12 @@ bool defer_supported(int bits, int act) { return bits == 4 || (bits == 8 && act 
 cudaError_t launch_gemm_defer(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
                               const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                               const CUtensorMap& b, const CUtensorMap& x, const GemmArgs& a) {
+  const int nt = a.block;
   if (bits == 4)
-    return gemm == 1 ? by_dtype<4, 1>(act, scl, grid, smem, stream, q, s, z, b, x, a)
-                     : by_dtype<4, 2>(act, scl, grid, smem, stream, q, s, z, b, x, a);
-  return gemm == 1 ? by_dtype<8, 1>(act, scl, grid, smem, stream, q, s, z, b, x, a)
-                   : by_dtype<8, 2>(act, scl, grid, smem, stream, q, s, z, b, x, a);
+    return gemm == 1 ? by_tile<4, 1>(nt, act, scl, grid, smem, stream, q, s, z, b, x, a)
+                     : by_tile<4, 2>(nt, act, scl, grid, smem, stream, q, s, z, b, x, a);
+  return gemm == 1 ? by_tile<8, 1>(nt, act, scl, grid, smem, stream, q, s, z, b, x, a)
+                   : by_tile<8, 2>(nt, act, scl, grid, smem, stream, q, s, z, b, x, a);
 }
 
 }  // namespace wna16

@@ -1,4 +1,4 @@
-// Grouped expert GEMM for decode-sized token tiles (16 tokens) with the
+// Grouped expert GEMM for decode-sized token tiles (16 or 32 tokens) with the
 // quantization scale and zero point taken out of the per-element work.
 //
 // For one 128-wide K stage of weight row n (one quantization group, or part of
@@ -44,7 +44,11 @@ namespace wna16 {
 constexpr int kDeferThreads = 10 * 32;
 // TMEM columns: P_0 [0,16), P_1 [16,32), C [32,48); A slot g at 64 + 96 g:
 // 64 columns for the 128 K of the stage, then 8 columns for the correction.
-constexpr int kDeferC = 2 * kDeferNT;
+// Combine buffer C: its own 16 columns at [32, 48) for 16-token tiles; for
+// 32-token tiles it is P_1 itself (the TMEM budget has no room for a third
+// 32-column buffer), which warpgroup 1 may reuse only after warpgroup 0 took C.
+template <int NT>
+__host__ __device__ constexpr int defer_c_col() { return NT == 16 ? 32 : NT; }
 constexpr int kDeferA0 = 64;
 constexpr int kDeferAStride = 96;
 constexpr int kDeferTmemCols = 256;
@@ -168,12 +172,12 @@ __device__ __forceinline__ float scale_to_f32(uint32_t bits) {
   else return __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(bits)));
 }
 
-template <int BITS, int ACT, int SCL, int GEMM>
+template <int BITS, int ACT, int SCL, int GEMM, int NT>
 __global__ void __launch_bounds__(kDeferThreads, 2)
     moe_gemm_defer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
                           const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_b,
                           const __grid_constant__ CUtensorMap tm_x, const GemmArgs a) {
-  constexpr int NT = kDeferNT;
+  static_assert(NT == 16 || NT == 32, "deferred-scale token tiles: 16 or 32");
   constexpr int PF = 32 / BITS;
   constexpr int KW = kTileK * BITS / 32;
   constexpr int W_BYTES = weight_code_bytes(BITS);
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t a_slot = tmem + t_lane + kDeferA0 + g * kDeferAStride;
     const uint32_t p_addr = tmem + t_lane + g * NT;
-    const uint32_t c_addr = tmem + t_lane + kDeferC;
+    const uint32_t c_addr = tmem + t_lane + defer_c_col<NT>();
     const bool builder = ((warp - 2) & 3) == 0 && lane < NT;  // first warp of the group writes the B rows
     uint8_t* my_bcorr = bcorr + g * NT * 128;
     const uint4* row_base = reinterpret_cast<const uint4*>(wring + srow * KW * 4);
@@ -423,11 +427,14 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         // this stage's partial sum, scaled into the accumulators
         if (!warp_wait_all(&pfull[g], pph, abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
-        uint32_t v[16];
-        tmem_ld16(p_addr, v);
-        tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < NT; ++j) acc[j] = fmaf(scale, __uint_as_float(v[j]), acc[j]);
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(p_addr + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(scale, __uint_as_float(v[j]), acc[c0 + j]);
+        }
         pph ^= 1u;
         cs += 2;
         if (cs >= NS) {
@@ -441,44 +448,50 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
       if (g == 1) {
         if (!warp_wait_all(cempty, (uc & 1) ^ 1, abort_flag, a.status)) break;
         tc_fence_after();
-        uint32_t v[16];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) v[j] = __float_as_uint(acc[j]);
-        tmem_st16(c_addr, v);
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+          uint32_t v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(acc[c0 + j]);
+          tmem_st16(c_addr + c0, v);
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(cfull);
+        // C aliases P_1: the next MMA into it must wait until warpgroup 0 took C
+        if (defer_c_col<NT>() == NT && !warp_wait_all(cempty, uc & 1, abort_flag, a.status)) break;
         continue;
       }
       if (!warp_wait_all(cfull, uc & 1, abort_flag, a.status)) break;
       tc_fence_after();
-      {
+#pragma unroll
+      for (int c0 = 0; c0 < NT; c0 += 16) {
         uint32_t v[16];
-        tmem_ld16(c_addr, v);
+        tmem_ld16(c_addr + c0, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < NT; ++j) acc[j] += __uint_as_float(v[j]);
+        for (int j = 0; j < 16; ++j) acc[c0 + j] += __uint_as_float(v[j]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cempty);
       if (GEMM == 1) {
         // silu(gate) * up -> act cache; lanes 0-15 hold gate rows, 16-31 the up
-        // rows of the same features: each lane finishes 8 of the 16 tokens.
+        // rows of the same features: each lane finishes half of the NT tokens.
         using T = typename Act<ACT>::T;
         T* act = reinterpret_cast<T*>(a.out);
         const bool lo = lane < 16;
         const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
         const int fp = kPermuteK<BITS> ? permute_k8(f) : f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float mine = lo ? acc[j] : acc[j + 8];
-          const float other = __shfl_xor_sync(0xFFFFFFFFu, lo ? acc[j + 8] : acc[j], 16);
+        for (int j = 0; j < NT / 2; ++j) {
+          const float mine = lo ? acc[j] : acc[j + NT / 2];
+          const float other = __shfl_xor_sync(0xFFFFFFFFu, lo ? acc[j + NT / 2] : acc[j], 16);
           const float gt = lo ? mine : other;
           const float up = lo ? other : mine;
           const float val = gt / (1.0f + __expf(-gt)) * up;
-          const int col = lo ? j : j + 8;
+          const int col = lo ? j : j + NT / 2;
           const size_t row = static_cast<size_t>(w.blk) * NT + col;
           float stored;
           if constexpr (ACT == 0) {
@@ -504,7 +517,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
       } else {
         float* slab = reinterpret_cast<float*>(a.out);
         const int hr = w.tile * kTileRows + q * 32 + lane;
-        const int my_pid = a.sorted_ids[w.blk * NT + (lane & 15)];
+        const int my_pid = a.sorted_ids[w.blk * NT + (lane & (NT - 1))];
         const float my_w = (my_pid >= 0 && my_pid < a.P) ? a.topk_w[my_pid] : 0.f;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -45,8 +46,30 @@ int choose_block_impl(int64_t M, int topk, int E) {
   const int64_t P = M * topk;
   if (P <= 0) return 16;
   const int64_t active = std::min<int64_t>(P, E);
-  const int64_t avg = (P + active - 1) / active;  // pairs per active expert
-  int b = 16;
+  const double avg = static_cast<double>(P) / static_cast<double>(active);  // pairs per active expert
+  if (avg <= 64.0) {
+    // Weight streaming dominates: every token block of an expert streams the
+    // expert's whole weights once. Pick the tile with the fewest streaming
+    // passes times the cost of one pass, measured on GB300 (Mixtral-8x7B
+    // gate/up): 16-token tiles 1.0, 32-token 1.28 (both the deferred-scale
+    // kernel), 64-token 1.34. Expert loads are uneven, so a block count of
+    // ceil(1.3 * avg / tile) is assumed.
+    const int tiles[3] = {16, 32, 64};
+    const double cost[3] = {1.0, 1.28, 1.34};
+    int best = 16;
+    double best_cost = 1e30;
+    for (int i = 0; i < 3; ++i) {
+      const double passes = std::ceil(1.3 * avg / tiles[i]);
+      if (passes * cost[i] < best_cost - 1e-9) {
+        best_cost = passes * cost[i];
+        best = tiles[i];
+      }
+    }
+    return best;
+  }
+  // Larger batches are tensor-bound: the smallest power of two covering the
+  // average, up to 128.
+  int b = 64;
   while (b < 128 && b < avg) b <<= 1;
   return b;
 }
@@ -84,9 +107,9 @@ Pipe pipe_for(int bits, int block) {
 }
 
 // Stages of the deferred-scale kernel (two CTAs per SM).
-int defer_stages(int bits, int gemm) {
+int defer_stages(int bits, int gemm, int nt) {
   int st = kMaxStages;
-  while (st > 2 && defer_smem_bytes(bits, gemm, st) > kHalfSmem) --st;
+  while (st > 2 && defer_smem_bytes(bits, gemm, nt, st) > kHalfSmem) --st;
   return st;
 }
 
@@ -126,7 +149,7 @@ WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, 
   // [H/128 stages][4][cap] and [I/128 stages][16][cap] floats
   const size_t kt1 = static_cast<size_t>((H + kTileK - 1) / kTileK);
   const size_t kt2 = static_cast<size_t>((I + kTileK - 1) / kTileK);
-  const bool defer = block == kDeferNT;
+  const bool defer = defer_tile(block);
   w.xs1 = take(defer ? kt1 * defer_xs_parts(1) * cap * 4 : 0);
   w.xs2 = take(defer ? kt2 * defer_xs_parts(2) * cap * 4 : 0);
   w.total = o;
@@ -230,11 +253,11 @@ bool make_token_map(CUtensorMap* m, const void* base, int64_t K, int64_t rows, i
 }
 
 // Token sums of a deferred-scale GEMM: fp32 [stages][parts][rows], box
-// {16 rows, parts, 1 stage}.
-bool make_xs_map(CUtensorMap* m, const float* base, int64_t rows, int parts, int stages) {
+// {block rows, parts, 1 stage}.
+bool make_xs_map(CUtensorMap* m, const float* base, int64_t rows, int parts, int stages, int block) {
   const uint64_t d[3] = {static_cast<uint64_t>(rows), static_cast<uint64_t>(parts), static_cast<uint64_t>(stages)};
   const uint64_t st[2] = {static_cast<uint64_t>(rows) * 4, static_cast<uint64_t>(rows) * parts * 4};
-  const uint32_t b[3] = {static_cast<uint32_t>(kDeferNT), static_cast<uint32_t>(parts), 1};
+  const uint32_t b[3] = {static_cast<uint32_t>(block), static_cast<uint32_t>(parts), 1};
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, 3, d, st, b);
 }
 
@@ -361,9 +384,10 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   const int64_t cap = capacity(P, E, B);
   const int max_blocks = static_cast<int>(cap / B);
   const bool zeros = w13_zeros != nullptr;
-  // 16-token tiles run the deferred-scale kernel when every stage lies in one
-  // group (G >= 128) and the code/activation formats have a magic-number form.
-  const bool defer = B == kDeferNT && r.G1 >= kTileK && r.G2 >= kTileK && defer_supported(bits, act_dtype);
+  // 16- and 32-token tiles run the deferred-scale kernel when every stage lies
+  // in one group (G >= 128) and the code/activation formats have a
+  // magic-number form.
+  const bool defer = defer_tile(B) && r.G1 >= kTileK && r.G2 >= kTileK && defer_supported(bits, act_dtype);
   const int kt1 = static_cast<int>((H + kTileK - 1) / kTileK);
   const int kt2 = static_cast<int>((I + kTileK - 1) / kTileK);
   float* xs1 = defer ? reinterpret_cast<float*>(ws + L.xs1) : nullptr;
@@ -382,8 +406,8 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   if (!make_token_map(&m1.b, x_sorted, H, cap, B) || !make_token_map(&m2.b, act, I, cap, B))
     return WNA16_ERR_CUDA;
   CUtensorMap x1{}, x2{};
-  if (defer && (!make_xs_map(&x1, xs1, cap, defer_xs_parts(1), kt1) ||
-                !make_xs_map(&x2, xs2, cap, defer_xs_parts(2), kt2)))
+  if (defer && (!make_xs_map(&x1, xs1, cap, defer_xs_parts(1), kt1, B) ||
+                !make_xs_map(&x2, xs2, cap, defer_xs_parts(2), kt2, B)))
     return WNA16_ERR_CUDA;
 
   if (!mark(0) || launch_align(topk_ids, P, E, B, static_cast<int>(cap), sorted, experts, npp, counts, status,
@@ -442,8 +466,8 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   if (!mark(2)) return WNA16_ERR_CUDA;
   cudaError_t e1;
   if (defer) {
-    a1.num_stages = defer_stages(bits, 1);
-    e1 = launch_gemm_defer(bits, act_dtype, scale_dtype, 1, grid1, defer_smem_bytes(bits, 1, a1.num_stages), s,
+    a1.num_stages = defer_stages(bits, 1, B);
+    e1 = launch_gemm_defer(bits, act_dtype, scale_dtype, 1, grid1, defer_smem_bytes(bits, 1, B, a1.num_stages), s,
                            m1.q, m1.s, m1.z, m1.b, x1, a1);
   } else {
     e1 = launch_gemm(bits, act_dtype, scale_dtype, 1, pipe.lean, grid1, pipe.smem, s, m1, a1);
@@ -465,8 +489,8 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   if (!mark(3)) return WNA16_ERR_CUDA;
   cudaError_t e2;
   if (defer) {
-    a2.num_stages = defer_stages(bits, 2);
-    e2 = launch_gemm_defer(bits, act_dtype, scale_dtype, 2, grid2, defer_smem_bytes(bits, 2, a2.num_stages), s,
+    a2.num_stages = defer_stages(bits, 2, B);
+    e2 = launch_gemm_defer(bits, act_dtype, scale_dtype, 2, grid2, defer_smem_bytes(bits, 2, B, a2.num_stages), s,
                            m2.q, m2.s, m2.z, m2.b, x2, a2);
   } else {
     e2 = launch_gemm(bits, act_dtype, scale_dtype, 2, pipe.lean, grid2, pipe.smem, s, m2, a2);
