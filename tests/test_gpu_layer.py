@@ -113,6 +113,19 @@ def test_deferred_scale_half_stage(bits, act):
     check(li, block=32, split_k=2)
 
 
+@pytest.mark.parametrize("M,block", [(1, 16), (3, 16), (2, 32)])
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_gate_up_k_split(M, block, act):
+    # few work units and K = 2048 (16 stages): the gate/up GEMM splits K in two;
+    # split units publish fp32 partial sums and the last one of each lane quarter
+    # adds them up before silu(gate) * up. Called twice: the arrival counters
+    # must start from zero again.
+    wl = small(H=2048, I=256, E=4, topk=1, group_size=128, act_dtype=act, scale_dtype=act)
+    li = make_layer_inputs(wl, M).to(DEV)
+    check(li, block=block)
+    check(li, block=block)
+
+
 def test_deferred_scale_large_activations():
     # hidden values 50x larger: the fp16 token sums of the correction operand
     # (stored at 1/32) and the magic-number offsets must not lose the result

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(256)
     moe_gather_kernel(const uint4* __restrict__ hidden, const int32_t* __restrict__ ids,
                       const int32_t* __restrict__ slot_of_pair, int P, int topk, int E, int h8, int permute,
                       uint4* __restrict__ x_sorted, float* __restrict__ xs, int cap, float* __restrict__ zero0,
-                      int zero_n0, float* __restrict__ zero1, int zero_n1) {
+                      int zero_n0, float* __restrict__ zero1, int zero_n1, float* __restrict__ zero2, int zero_n2) {
   const int chunks = h8 / 8;
   const long long n = static_cast<long long>(P) * chunks;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(256)
   }
   for (long long i = first; i < zero_n0; i += stride) zero0[i] = 0.f;
   for (long long i = first; i < zero_n1; i += stride) zero1[i] = 0.f;
+  for (long long i = first; i < zero_n2; i += stride) zero2[i] = 0.f;
 }
 
 template <typename T>
@@ -267,10 +268,10 @@ cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, i
 cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
                           int topk, int E, int H, int permute, int act_dtype, int max_ctas, void* x_sorted,
                           float* xs, int cap, float* zero_ptr0, int zero_n0, float* zero_ptr1, int zero_n1,
-                          cudaStream_t stream) {
+                          float* zero_ptr2, int zero_n2, cudaStream_t stream) {
   const int h8 = H / 8;
   long long n = static_cast<long long>(P) * (h8 / 8);
-  n = std::max<long long>(n, std::max(zero_n0, zero_n1));
+  n = std::max<long long>(n, std::max({zero_n0, zero_n1, zero_n2}));
   const int threads = 256;
   const long long want = (n + threads - 1) / threads;
   const unsigned blocks = static_cast<unsigned>(want < max_ctas ? want : max_ctas);
@@ -278,11 +279,13 @@ cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t*
   if (act_dtype == 0)
     moe_gather_kernel<0><<<blocks, threads, 0, stream>>>(static_cast<const uint4*>(hidden), ids, slot_of_pair, P,
                                                          topk, E, h8, permute, static_cast<uint4*>(x_sorted), xs,
-                                                         cap, zero_ptr0, zero_n0, zero_ptr1, zero_n1);
+                                                         cap, zero_ptr0, zero_n0, zero_ptr1, zero_n1, zero_ptr2,
+                                                         zero_n2);
   else
     moe_gather_kernel<1><<<blocks, threads, 0, stream>>>(static_cast<const uint4*>(hidden), ids, slot_of_pair, P,
                                                          topk, E, h8, permute, static_cast<uint4*>(x_sorted), xs,
-                                                         cap, zero_ptr0, zero_n0, zero_ptr1, zero_n1);
+                                                         cap, zero_ptr0, zero_n0, zero_ptr1, zero_n1, zero_ptr2,
+                                                         zero_n2);
   return cudaGetLastError();
 }
 

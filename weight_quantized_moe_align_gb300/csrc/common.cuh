@@ -66,6 +66,8 @@ struct GemmArgs {
   int num_acc;
   uint32_t tmem_cols;
   float* xs_out;               // deferred-scale gate/up GEMM: token sums of the act cache per down stage
+  float* part;                 // deferred-scale gate/up GEMM with split > 1: [tile][block][split][128][nt] fp32
+  int* counters;               //   arrivals per (tile, block, lane quarter), zero between calls
   int cap;                     // rows of the expert-sorted token matrices
 };
 

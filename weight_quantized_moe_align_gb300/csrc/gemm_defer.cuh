@@ -476,6 +476,38 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cempty);
+      if (GEMM == 1 && a.split > 1) {
+        // K split: each split unit publishes its fp32 partial sums; per lane
+        // quarter, the last of the split units to arrive adds them up in split
+        // order (deterministic) and runs the epilogue. The others stop here.
+        const size_t unit_base = (static_cast<size_t>(w.tile) * a.max_blocks + w.blk) * a.split;
+        const int row = q * 32 + lane;  // TMEM lane = row of the 128-row tile
+        float4* mine = reinterpret_cast<float4*>(a.part + ((unit_base + w.sp) * kTileRows + row) * NT);
+#pragma unroll
+        for (int j = 0; j < NT; j += 4) mine[j / 4] = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+        __threadfence();
+        __syncwarp();
+        int* counter = a.counters + (static_cast<size_t>(w.tile) * a.max_blocks + w.blk) * 4 + q;
+        int arrived = 0;
+        if (lane == 0) arrived = atomicAdd(counter, 1);
+        arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
+        if (arrived != a.split - 1) continue;
+        __threadfence();
+#pragma unroll
+        for (int j = 0; j < NT; ++j) acc[j] = 0.f;
+        for (int sp = 0; sp < a.split; ++sp) {
+          const float4* src = reinterpret_cast<const float4*>(a.part + ((unit_base + sp) * kTileRows + row) * NT);
+#pragma unroll
+          for (int j = 0; j < NT; j += 4) {
+            const float4 v4 = __ldcg(src + j / 4);
+            acc[j] += v4.x;
+            acc[j + 1] += v4.y;
+            acc[j + 2] += v4.z;
+            acc[j + 3] += v4.w;
+          }
+        }
+        if (lane == 0) *counter = 0;  // ready for the next call
+      }
       if (GEMM == 1) {
         // silu(gate) * up -> act cache; lanes 0-15 hold gate rows, 16-31 the up
         // rows of the same features: each lane finishes half of the NT tokens.

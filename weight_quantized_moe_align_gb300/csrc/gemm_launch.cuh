@@ -23,12 +23,13 @@ cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, i
                          int32_t* expert_ids, int32_t* num_post_pad, int32_t* counts,
                          int32_t* status, int32_t* slot_of_pair, cudaStream_t stream);
 // Expert-sorted copy of the hidden rows; with `xs` also the deferred-scale
-// token sums [H/128 stages][4 parts][cap] and zeros for the `zero_n` floats at
-// each `zero_ptr` (token-sum parts of a stage half with no K elements).
+// token sums [H/128 stages][4 parts][cap]. It also zeroes the `zero_n` 32-bit
+// words at each `zero_ptr` (token-sum parts of a stage half with no K
+// elements, the gate/up GEMM's split arrival counters).
 cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
                           int topk, int E, int H, int permute, int act_dtype, int max_ctas, void* x_sorted,
                           float* xs, int cap, float* zero_ptr0, int zero_n0, float* zero_ptr1, int zero_n1,
-                          cudaStream_t stream);
+                          float* zero_ptr2, int zero_n2, cudaStream_t stream);
 cudaError_t launch_combine(const float* slab, const int32_t* ids, int M, int H, int topk, int E,
                            int split, int act_dtype, void* out, cudaStream_t stream);
 

@@ -113,20 +113,36 @@ int defer_stages(int bits, int gemm, int nt) {
   return st;
 }
 
+// Expected token blocks of a batch (the host does not see the routing): the
+// active experts times the blocks an expert of average load needs. The
+// capacity bound would overcount the padding.
+int64_t expected_blocks(int64_t M, int topk, int E, int block) {
+  const int64_t P = M * topk;
+  if (P <= 0) return 0;
+  const int64_t active = std::min<int64_t>(P, E);
+  const int64_t avg = (P + active - 1) / active;
+  return active * ((avg + block - 1) / block);
+}
+
+// K split of a GEMM launch: only when the units do not fill the persistent CTA
+// slots, then as many splits as fit (at most 8, keeping >= 8 K stages per
+// split). Finer splits that merely even out the rounds were measured slower:
+// every unit boundary stalls the dequant chain (accumulator handoff, epilogue,
+// and for the gate/up GEMM the partial-sum exchange).
 int choose_split(int64_t units, int kt_total, int ctas_per_sm) {
-  const int slots = sm_count() * ctas_per_sm;
+  const int64_t slots = static_cast<int64_t>(sm_count()) * ctas_per_sm;
   if (units >= slots) return 1;
   int s = static_cast<int>(slots / std::max<int64_t>(units, 1));
   s = std::min(s, 8);
-  s = std::min(s, std::max(1, kt_total / 8));  // keep >= 8 K stages per split
+  s = std::min(s, std::max(1, kt_total / 8));
   return std::max(s, 1);
 }
 
 struct WsLayout {
-  size_t status, sorted, experts, npp, counts, slot_of_pair, x_sorted, act, slab, xs1, xs2, total;
+  size_t status, sorted, experts, npp, counts, slot_of_pair, x_sorted, act, slab, xs1, xs2, part1, cnt1, total;
 };
 
-WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, int split) {
+WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, int split, int split1) {
   const int64_t P = M * topk;
   const int64_t cap = capacity(P, E, block);
   WsLayout w;
@@ -152,6 +168,11 @@ WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, 
   const bool defer = defer_tile(block);
   w.xs1 = take(defer ? kt1 * defer_xs_parts(1) * cap * 4 : 0);
   w.xs2 = take(defer ? kt2 * defer_xs_parts(2) * cap * 4 : 0);
+  // K-split partial sums of the deferred-scale gate/up GEMM and their arrival
+  // counters: [I/64 tiles][cap/block][split1][128][block] floats, [I/64][cap/block][4] ints
+  const size_t tiles1 = static_cast<size_t>(I / kGateUpRows), blocks = static_cast<size_t>(cap / block);
+  w.part1 = take(split1 > 1 ? tiles1 * blocks * split1 * kTileRows * block * 4 : 0);
+  w.cnt1 = take(split1 > 1 ? tiles1 * blocks * 4 * 4 : 0);
   w.total = o;
   return w;
 }
@@ -268,7 +289,7 @@ cudaError_t launch_gemm(int bits, int act, int scl, int gemm, int lean, dim3 gri
 }
 
 struct Resolved {
-  int block, split, G1, G2;
+  int block, split, split1, G1, G2;
 };
 
 wna16_status resolve(int64_t M, int64_t H, int64_t I, int E, int topk, int bits, int group_size,
@@ -296,11 +317,19 @@ wna16_status resolve(int64_t M, int64_t H, int64_t I, int E, int topk, int bits,
   if (split_k < 0 || split_k > 8) return WNA16_ERR_INVALID_ARG;
   const int kt2 = static_cast<int>((I + kTileK - 1) / kTileK);
   if (split_k == 0) {
-    const int64_t blocks = capacity(M * topk, E, block) / block;
-    const int64_t units = blocks * ((H + kTileRows - 1) / kTileRows);
+    const int64_t units = expected_blocks(M, topk, E, block) * ((H + kTileRows - 1) / kTileRows);
     split_k = choose_split(units, kt2, pipe_for(bits, block).ctas_per_sm);
   }
   r->split = std::min(split_k, kt2);
+  // gate/up GEMM: K split only on the deferred-scale path (token tiles of 16 or
+  // 32 with groups of >= 128); automatic
+  r->split1 = 1;
+  const int G1 = r->G1;
+  if (defer_tile(block) && G1 >= kTileK && r->G2 >= kTileK) {
+    const int kt1 = static_cast<int>((H + kTileK - 1) / kTileK);
+    const int64_t units1 = expected_blocks(M, topk, E, block) * (I / kGateUpRows);
+    r->split1 = choose_split(units1, kt1, 2);
+  }
   return WNA16_OK;
 }
 
@@ -338,7 +367,7 @@ size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, i
                                        int group_size, int block, int split_k) {
   Resolved r;
   if (resolve(M, H, I, E, topk, bits, group_size, block, split_k, &r) != WNA16_OK) return 0;
-  return ws_layout(M, H, I, E, topk, r.block, r.split).total;
+  return ws_layout(M, H, I, E, topk, r.block, r.split, r.split1).total;
 }
 
 wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
@@ -364,7 +393,7 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
     if (p && !aligned16(p)) return WNA16_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_weights) & 3u))
     return WNA16_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(M, H, I, E, topk, r.block, r.split);
+  const WsLayout L = ws_layout(M, H, I, E, topk, r.block, r.split, r.split1);
   if (workspace_bytes < L.total) return WNA16_ERR_WORKSPACE_TOO_SMALL;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -425,9 +454,14 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
     zero2 = xs2 + (static_cast<size_t>(kt2 - 1) * 16 + 8) * cap;
     zero2_n = static_cast<int>(8 * cap);
   }
+  // K split of the deferred-scale gate/up GEMM: its arrival counters start at zero
+  const int split1 = defer ? r.split1 : 1;
+  float* part1 = split1 > 1 ? reinterpret_cast<float*>(ws + L.part1) : nullptr;
+  int* cnt1 = split1 > 1 ? reinterpret_cast<int*>(ws + L.cnt1) : nullptr;
+  const int cnt1_n = split1 > 1 ? static_cast<int>((I / kGateUpRows) * max_blocks * 4) : 0;
   if (!mark(1) || launch_gather(hidden, topk_ids, slot_of_pair, P, topk, E, static_cast<int>(H), bits == 4 ? 1 : 0,
                                 act_dtype, sm_count() * 8, x_sorted, xs1, static_cast<int>(cap), zero1, zero1_n,
-                                zero2, zero2_n, s) != cudaSuccess)
+                                zero2, zero2_n, reinterpret_cast<float*>(cnt1), cnt1_n, s) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
   const Pipe pipe = pipe_for(bits, B);
@@ -451,7 +485,7 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a1.groups = static_cast<int>(H / r.G1);
   a1.G = r.G1;
   a1.kt_total = static_cast<int>((H + kTileK - 1) / kTileK);
-  a1.split = 1;
+  a1.split = split1;
   a1.has_zeros = zeros ? 1 : 0;
   a1.max_blocks = max_blocks;
   a1.num_stages = pipe.stages;
@@ -460,7 +494,9 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a1.tmem_cols = pipe.tmem_cols;
   a1.xs_out = xs2;
   a1.cap = static_cast<int>(cap);
-  const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles;
+  a1.part = part1;
+  a1.counters = cnt1;
+  const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles * split1;
   const int64_t slots = static_cast<int64_t>(sms) * pipe.ctas_per_sm;
   const dim3 grid1(static_cast<unsigned>(std::min<int64_t>(units1, slots)));
   if (!mark(2)) return WNA16_ERR_CUDA;
