@@ -438,30 +438,26 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
       hrow = srow;
     }
     const uint32_t t_lane = (q * 32) << 16;
-    // Running positions (stage index it, its ring slot s and phase, A slot,
-    // and the stage it - NA whose completion frees that A slot), advanced for
-    // every stage so both warpgroups agree on them.
-    int it = 0, s = 0, slot = 0, ps = NS - NA;  // ps = (it - NA) mod NS
-    int uc = 0;                                 // units finished (epilogue count, LEAN)
-    uint32_t f_phase = 0, p_phase = 1;          // p_phase: phase of stage it - NA (unused while it < NA)
+    // This group's stages are the running stage indices gi = grp, grp + step,
+    // ... across units (step 2, or 1 for LEAN). Tracked incrementally: the ring
+    // slot cs and phase cf of stage gi, its A slot cslot, and the ring slot cps
+    // and phase cp of stage gi - NA, whose completed MMAs free that A slot
+    // (floor division, so the tracking stays consistent through gi < NA).
+    constexpr int step = LEAN ? 1 : 2;
+    const int pfirst = grp - NA;
+    int cs = grp % NS, cslot = grp % NA, gi = grp;
+    int cps = ((pfirst % NS) + NS) % NS;
+    uint32_t cf = (grp / NS) & 1u;
+    uint32_t cp = static_cast<uint32_t>((pfirst >= 0 ? pfirst / NS : (pfirst - NS + 1) / NS) & 1);
+    int it = 0;  // running index of the current unit's first stage
+    int uc = 0;  // units finished (epilogue count, LEAN)
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = decode_unit(u, nb, a);
+      const int n = w.kt1 - w.kt0;
       bool ok = true;
-      for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
-        const int cs = s, cslot = slot, cps = ps;
-        const uint32_t cf = f_phase, cp = p_phase;
-        if (++s == NS) {
-          s = 0;
-          f_phase ^= 1u;
-        }
-        if (++slot == NA) slot = 0;
-        if (++ps == NS) {
-          ps = 0;
-          p_phase ^= 1u;
-        }
-        if (!LEAN && (it & 1) != grp) continue;
+      for (; gi < it + n; gi += step) {
         if (!warp_wait_all(&full[cs], cf, abort_flag, a.status)) { ok = false; break; }
-        if (it >= NA) {
+        if (gi >= NA) {
           if (!warp_wait_all(&empty[cps], cp, abort_flag, a.status)) { ok = false; break; }
         }
         const uint8_t* st = wring + cs * WST;
@@ -503,7 +499,20 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[cslot]);
+        cs += step;
+        if (cs >= NS) {
+          cs -= NS;
+          cf ^= 1u;
+        }
+        cps += step;
+        if (cps >= NS) {
+          cps -= NS;
+          cp ^= 1u;
+        }
+        cslot += step;
+        if (cslot >= NA) cslot -= NA;
       }
+      it += n;
       if (!ok) break;
       if (LEAN) {
         // this warpgroup also runs the epilogue, right after the unit's last stage
