@@ -141,10 +141,11 @@ struct Dequant {
             out[i * 4 + j] = pack2_rn<ACT>(f0, f1);
           }
         } else {
+          // one prmt puts byte c into the low mantissa bits of 2^23 (0x4B0000uu)
 #pragma unroll
           for (int c = 0; c < 4; c += 2) {
-            const float f0 = code_minus_zero((x >> (8 * c)) & MASK, mz) * s;
-            const float f1 = code_minus_zero((x >> (8 * (c + 1))) & MASK, mz) * s;
+            const float f0 = (__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440 + c)) - mz) * s;
+            const float f1 = (__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440 + c + 1)) - mz) * s;
             out[(i * 4 + c) / 2] = pack2_rn<ACT>(f0, f1);
           }
         }
