@@ -136,6 +136,15 @@ def test_deferred_scale_large_activations():
     check(li, block=32)
 
 
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_int8_256_token_tiles_single_a_slot(act):
+    # 8-bit codes with 256-token tiles leave room for two ring stages and so a
+    # single TMEM A slot: the two dequant warpgroups must take turns on it
+    wl = small(bits=8, has_zeros=False, group_size=-1, act_dtype=act, scale_dtype="f16", H=384, I=256, E=2, topk=1)
+    li = make_layer_inputs(wl, 300).to(DEV)
+    check(li, block=256)
+
+
 def test_hidden_not_multiple_of_row_tile():
     # H = 320: the down GEMM's last 128-row tile is half outside the matrix
     li = make_layer_inputs(small(H=320, I=128, group_size=64), 11).to(DEV)

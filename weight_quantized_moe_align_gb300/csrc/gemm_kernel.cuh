@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     // slot cs and phase cf of stage gi, its A slot cslot, and the ring slot cps
     // and phase cp of stage gi - NA, whose completed MMAs free that A slot
     // (floor division, so the tracking stays consistent through gi < NA).
-    constexpr int step = LEAN ? 1 : 2;
+    constexpr int step = LEAN ? 1 : 2;  // the ring has NS >= 2 stages, so one wrap suffices for cs, cps
     const int pfirst = grp - NA;
     int cs = grp % NS, cslot = grp % NA, gi = grp;
     int cps = ((pfirst % NS) + NS) % NS;
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
           cp ^= 1u;
         }
         cslot += step;
-        if (cslot >= NA) cslot -= NA;
+        while (cslot >= NA) cslot -= NA;  // NA may be 1 (two 256-token stages): then always slot 0
       }
       it += n;
       if (!ok) break;
