@@ -61,6 +61,7 @@ struct GemmArgs {
   int split;                   // K splits (down GEMM), 1 otherwise
   int has_zeros;
   int max_blocks;              // cap / block
+  int panel;                   // token blocks per panel of the work-unit order
   int num_stages;
   int num_aslots;
   int num_acc;

@@ -158,12 +158,23 @@ struct Unit {
   int blk, tile, sp, kt0, kt1;
 };
 
+// Work-unit order (the same in every role): panels of a.panel consecutive
+// token blocks (the align output is expert-sorted, so a panel spans one or a
+// few experts); inside a panel the weight tile is the slowest index and the K
+// split the fastest. Concurrent CTAs then share a panel's token rows and each
+// weight tile across the panel's blocks. The host sizes panels so that their
+// token rows stay well inside L2; small batches get one panel.
 __device__ __forceinline__ Unit decode_unit(int u, int nb, const GemmArgs& a) {
   Unit r;
-  r.blk = u % nb;
-  const int rest = u / nb;
+  const int panel_units = a.panel * a.n_tiles * a.split;
+  const int p = u / panel_units;
+  const int b0 = p * a.panel;
+  const int pbs = nb - b0 < a.panel ? nb - b0 : a.panel;  // blocks in this panel
+  int rest = u - p * panel_units;
   r.sp = rest % a.split;
-  r.tile = rest / a.split;
+  rest /= a.split;
+  r.blk = b0 + rest % pbs;
+  r.tile = rest / pbs;
   r.kt0 = static_cast<int>(static_cast<long long>(a.kt_total) * r.sp / a.split);
   r.kt1 = static_cast<int>(static_cast<long long>(a.kt_total) * (r.sp + 1) / a.split);
   return r;

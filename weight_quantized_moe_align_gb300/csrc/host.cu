@@ -113,6 +113,15 @@ int defer_stages(int bits, int gemm, int nt) {
   return st;
 }
 
+// Token blocks per panel of the GEMM work-unit order: as many as keep their
+// token rows (block x K x 2 bytes) within about a third of the L2.
+int panel_blocks(int block, int64_t K, int max_blocks) {
+  const int64_t budget = 48ll << 20;
+  const int64_t per_block = static_cast<int64_t>(block) * K * 2;
+  const int64_t p = std::max<int64_t>(1, budget / std::max<int64_t>(per_block, 1));
+  return static_cast<int>(std::min<int64_t>(p, std::max(max_blocks, 1)));
+}
+
 // Expected token blocks of a batch (the host does not see the routing): the
 // active experts times the blocks an expert of average load needs. The
 // capacity bound would overcount the padding.
@@ -488,6 +497,7 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a1.split = split1;
   a1.has_zeros = zeros ? 1 : 0;
   a1.max_blocks = max_blocks;
+  a1.panel = panel_blocks(B, H, max_blocks);
   a1.num_stages = pipe.stages;
   a1.num_aslots = pipe.aslots;
   a1.num_acc = pipe.acc;
@@ -517,6 +527,7 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a2.I = 0;
   a2.n_tiles = static_cast<int>((H + kTileRows - 1) / kTileRows);
   a2.groups = static_cast<int>(I / r.G2);
+  a2.panel = panel_blocks(B, I, max_blocks);
   a2.G = r.G2;
   a2.kt_total = static_cast<int>((I + kTileK - 1) / kTileK);
   a2.split = r.split;
