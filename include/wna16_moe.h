@@ -216,6 +216,41 @@ wna16_status wna16_fused_moe_noalloc(const void* hidden, wna16_dtype act_dtype, 
                                      void* stream);
 
 /*
+ * Prepacked weights (optional, a one-time conversion at load time).
+ *
+ * The GPTQ-Marlin kernels of vLLM PR #14138 run on weights repacked offline
+ * into the kernel's own tile order; this is the same idea for this library.
+ * wna16_prepack rewrites one projection (w13 or w2) from the plain layout above
+ * into stage images: for every (expert, 128-row tile, 128-wide K stage), one
+ * contiguous block that is byte-identical to the shared-memory stage the GEMM
+ * kernels assemble from the plain layout (codes in their swizzled order, then
+ * the stage's scales, then its zero points). The fused call then moves each
+ * stage with one contiguous bulk copy instead of three strided tiled copies;
+ * the arithmetic, and so the output, is unchanged (bit-identical).
+ *
+ *   wna16_prepack_bytes: size of the packed form of one projection with
+ *     (N, K) = (2I, H), gate_up = 1 for w13, or (H, I), gate_up = 0 for w2;
+ *     0 for unsupported shapes (same rules as wna16_fused_moe).
+ *   wna16_prepack: q / scales / zeros (zeros may be NULL) in the plain layout
+ *     -> dst (device, 16-byte aligned, wna16_prepack_bytes() bytes). One launch
+ *     on `stream`; the inputs may be freed once it completed.
+ *   wna16_fused_moe_prepacked: wna16_fused_moe on packed w13 and w2 (both made
+ *     with the same bits, group_size and zero-point presence, has_zeros = 1 if
+ *     they carry zero points). Same workspace size, errors and semantics;
+ *     `events` as in wna16_fused_moe_timed (may be NULL).
+ */
+size_t wna16_prepack_bytes(int E, int64_t N, int64_t K, int bits, int group_size, int has_zeros, int gate_up);
+wna16_status wna16_prepack(const int32_t* q, const void* scales, const int32_t* zeros, int E, int64_t N,
+                           int64_t K, int bits, int group_size, int gate_up, void* dst, void* stream);
+wna16_status wna16_fused_moe_prepacked(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
+                                       int64_t I, int E, int topk, const void* w13_packed,
+                                       const void* w2_packed, int has_zeros, wna16_dtype scale_dtype,
+                                       int bits, int group_size, const int32_t* topk_ids,
+                                       const float* topk_weights, void* out, void* workspace,
+                                       size_t workspace_bytes, int block, int split_k, void* stream,
+                                       void* const* events);
+
+/*
  * Synchronizes `stream`, then reads the device status word at the start of a
  * fused-call workspace (or any int32 status word the caller passed to the
  * align call). Writes the raw bits to *bits_out (may be NULL) and returns

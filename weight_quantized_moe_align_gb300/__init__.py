@@ -5,13 +5,16 @@ from .binding import (  # noqa: F401
     DEV_BAD_EXPERT_ID,
     DEV_TIMEOUT,
     EXPORTED,
+    PackedWeights,
     WNA16Error,
     align_capacity,
     choose_block,
     fused_moe,
     fused_moe_noalloc,
+    fused_moe_prepacked,
     load,
     moe_align_block_size,
+    prepack,
     read_device_status,
     workspace_bytes,
 )

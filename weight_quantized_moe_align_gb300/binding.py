@@ -30,8 +30,8 @@ DEV_TIMEOUT = 0x2
 EXPORTED = (
     "wna16_align_capacity", "wna16_moe_align_block_size", "wna16_choose_block",
     "wna16_fused_moe_workspace_bytes", "wna16_fused_moe", "wna16_fused_moe_timed",
-    "wna16_fused_moe_noalloc", "wna16_read_device_status",
-    "wna16_status_string",
+    "wna16_fused_moe_noalloc", "wna16_prepack_bytes", "wna16_prepack", "wna16_fused_moe_prepacked",
+    "wna16_read_device_status", "wna16_status_string",
 )
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
@@ -72,6 +72,13 @@ def load() -> ctypes.CDLL:
     L.wna16_fused_moe_timed.restype = i32
     L.wna16_fused_moe_noalloc.argtypes = L.wna16_fused_moe.argtypes[:19] + [i32, i32, vp]
     L.wna16_fused_moe_noalloc.restype = i32
+    L.wna16_prepack_bytes.argtypes = [i32, i64, i64, i32, i32, i32, i32]
+    L.wna16_prepack_bytes.restype = sz
+    L.wna16_prepack.argtypes = [vp, vp, vp, i32, i64, i64, i32, i32, i32, vp, vp]
+    L.wna16_prepack.restype = i32
+    L.wna16_fused_moe_prepacked.argtypes = [vp, i32, i64, i64, i64, i32, i32, vp, vp, i32, i32, i32, i32, vp, vp,
+                                            vp, vp, sz, i32, i32, vp, vp]
+    L.wna16_fused_moe_prepacked.restype = i32
     L.wna16_read_device_status.argtypes = [vp, c.POINTER(c.c_int32), vp]
     L.wna16_read_device_status.restype = i32
     L.wna16_status_string.argtypes = [i32]
@@ -234,6 +241,78 @@ def fused_moe_noalloc(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: tor
         _ptr(w13_zeros), _ptr(w2_q), _ptr(w2_scales), _ptr(w2_zeros), _DTYPE[w13_scales.dtype], bits,
         group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out), block, split_k, _stream(stream))
     _raise(st, "wna16_fused_moe_noalloc")
+    return out
+
+
+class PackedWeights:
+    """One projection's weights in the prepacked stage-image form (see the
+    header): ``data`` (uint8, device) plus the shape information the fused call
+    needs."""
+
+    def __init__(self, data: torch.Tensor, E: int, N: int, K: int, bits: int, group_size: int,
+                 has_zeros: bool, scale_dtype: torch.dtype, gate_up: bool):
+        self.data, self.E, self.N, self.K = data, E, N, K
+        self.bits, self.group_size, self.has_zeros = bits, group_size, has_zeros
+        self.scale_dtype, self.gate_up = scale_dtype, gate_up
+
+
+def prepack(q: torch.Tensor, scales: torch.Tensor, zeros: Optional[torch.Tensor], bits: int, group_size: int,
+            gate_up: bool, stream=None) -> PackedWeights:
+    """``wna16_prepack`` of one projection: w13 (``gate_up=True``, q [E, 2I, H/pf])
+    or w2 (q [E, H, I/pf]) with its scales and zero points (or None)."""
+    _check(q, "q", torch.int32)
+    dev = q.device
+    E, N, kw = q.shape
+    K = kw * (32 // bits)
+    _check(scales, "scales", (torch.float16, torch.bfloat16), device=dev)
+    if zeros is not None:
+        _check(zeros, "zeros", torch.int32, device=dev)
+    n = int(load().wna16_prepack_bytes(E, N, K, bits, group_size, int(zeros is not None), int(gate_up)))
+    if n == 0:
+        raise WNA16Error(2, "wna16_prepack_bytes")
+    dst = torch.empty(n, dtype=torch.uint8, device=dev)
+    st = load().wna16_prepack(_ptr(q), _ptr(scales), _ptr(zeros), E, N, K, bits, group_size, int(gate_up),
+                              _ptr(dst), _stream(stream))
+    _raise(st, "wna16_prepack")
+    return PackedWeights(dst, E, N, K, bits, group_size, zeros is not None, scales.dtype, gate_up)
+
+
+def fused_moe_prepacked(hidden: torch.Tensor, w13: PackedWeights, w2: PackedWeights, topk_ids: torch.Tensor,
+                        topk_weights: torch.Tensor, out: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, block: int = 0, split_k: int = 0,
+                        stream=None, events=None) -> torch.Tensor:
+    """The fused layer on prepacked weights (``wna16_fused_moe_prepacked``)."""
+    _check(hidden, "hidden", (torch.float16, torch.bfloat16))
+    dev = hidden.device
+    M, H = hidden.shape
+    if not (w13.gate_up and not w2.gate_up):
+        raise ValueError("w13 must be the gate/up projection and w2 the down projection")
+    E, I = w13.E, w13.N // 2
+    if (w13.K, w2.N, w2.K, w2.E) != (H, H, I, E) or (w13.bits, w13.group_size, w13.has_zeros) != (
+            w2.bits, w2.group_size, w2.has_zeros) or w13.scale_dtype != w2.scale_dtype:
+        raise ValueError("w13 and w2 packed with inconsistent shapes or formats")
+    _check(w13.data, "w13.data", torch.uint8, device=dev)
+    _check(w2.data, "w2.data", torch.uint8, device=dev)
+    topk = topk_ids.shape[1] if topk_ids.dim() == 2 else -1
+    _check(topk_ids, "topk_ids", torch.int32, (M, topk), dev)
+    _check(topk_weights, "topk_weights", torch.float32, (M, topk), dev)
+    if out is None:
+        out = torch.empty_like(hidden)
+    _check(out, "out", hidden.dtype, (M, H), dev)
+    need = workspace_bytes(M, H, I, E, topk, w13.bits, w13.group_size, block, split_k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", torch.uint8, device=dev)
+    arr = None
+    if events is not None:
+        if len(events) != 6:
+            raise ValueError("events must hold 6 entries")
+        arr = (ctypes.c_void_p * 6)(*[None if e is None else e.cuda_event for e in events])
+    st = load().wna16_fused_moe_prepacked(
+        _ptr(hidden), _DTYPE[hidden.dtype], M, H, I, E, topk, _ptr(w13.data), _ptr(w2.data), int(w13.has_zeros),
+        _DTYPE[w13.scale_dtype], w13.bits, w13.group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out),
+        _ptr(workspace), workspace.numel(), block, split_k, _stream(stream), arr)
+    _raise(st, "wna16_fused_moe_prepacked")
     return out
 
 

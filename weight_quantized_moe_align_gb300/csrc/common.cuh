@@ -62,6 +62,8 @@ struct GemmArgs {
   int has_zeros;
   int max_blocks;              // cap / block
   int panel;                   // token blocks per panel of the work-unit order
+  const uint8_t* wpack;        // prepacked weights (stage images), or null: TMA boxes from the plain layout
+  int wimg;                    // bytes of one stage image
   int num_stages;
   int num_aslots;
   int num_acc;
@@ -82,6 +84,18 @@ __host__ __device__ constexpr int weight_ring_bytes(int bits, int stages) {
   return (stages * weight_stage_bytes(bits) + 1023) / 1024 * 1024;
 }
 __host__ __device__ constexpr int token_stage_bytes(int block) { return (kTileK / kChunkK) * block * 128; }
+
+// Prepacked weights (wna16_prepack): for every (expert, 128-row tile, 128-wide
+// K stage) one contiguous image, byte-identical to the shared-memory stage the
+// TMA boxes of the plain layout produce (same swizzle, zero fill outside the
+// matrix): codes, then the stage's group rows of scales (sg x 256 B), then
+// their zero points (sg x 128/pf x 4 B) if the weights have them. sg = 2 for
+// G = 64, else 1 (a group of G > 128 repeats its scales in each of its stages).
+__host__ __device__ constexpr int prepack_sg(int group_size_or_k) { return group_size_or_k == 64 ? 2 : 1; }
+__host__ __device__ constexpr int prepack_image_bytes(int bits, int sg, int has_zeros) {
+  return weight_code_bytes(bits) + sg * 256 + (has_zeros ? sg * (kTileRows * bits / 32) * 4 : 0);
+}
+
 
 // Fixed extras after the two rings: barriers and flags.
 __host__ __device__ constexpr int gemm_extra_bytes() { return 8 * (2 * kMaxStages + kMaxASlots + 4 + 1) + 64; }

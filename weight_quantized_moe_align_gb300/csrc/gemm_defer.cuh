@@ -225,11 +225,13 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_s);
+    if (!a.wpack) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_s);
+      if (a.has_zeros) prefetch_tmap(&tm_z);
+    }
     prefetch_tmap(&tm_b);
     prefetch_tmap(&tm_x);
-    if (a.has_zeros) prefetch_tmap(&tm_z);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, kDeferTmemCols);
@@ -246,7 +248,8 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    const uint32_t stage_tx = W_BYTES + 256 + (a.has_zeros ? (kTileRows / PF) * 4 : 0) + BST + XST;
+    const uint32_t stage_tx =
+        (a.wpack ? a.wimg : W_BYTES + 256 + (a.has_zeros ? (kTileRows / PF) * 4 : 0)) + BST + XST;
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_b = l2_policy_evict_last();
     int it = 0, s = 0;
@@ -265,7 +268,12 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         if (elect_one()) {
           mbar_arrive_expect_tx(&full[s], stage_tx);
           uint8_t* dst = wring + s * WST;
-          if (GEMM == 1) {
+          if (a.wpack) {
+            // prepacked: the stage's codes, scales and zero points as one image
+            const uint8_t* src =
+                a.wpack + ((static_cast<size_t>(e) * a.n_tiles + w.tile) * a.kt_total + kt) * a.wimg;
+            bulk_load(dst, src, a.wimg, &full[s], pol_w);
+          } else if (GEMM == 1) {
             const int f0 = w.tile * kGateUpRows;
             tma_load_3d(dst, &tm_q, &full[s], kt * KW, f0, 2 * e, pol_w);
             tma_load_3d(dst + S_OFF, &tm_s, &full[s], f0, 0, ys, pol_w);
@@ -354,6 +362,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     const int si = GEMM == 1 ? half * kGateUpRows + hrow : hrow;
     const int zi = GEMM == 1 ? half * (kGateUpRows / PF) + hrow / PF : hrow / PF;
     const int zshift = BITS * (hrow % PF);
+    const int z_off = a.wpack ? W_BYTES + 256 : Z_OFF;  // zero points: right after the scales in an image
     const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t a_slot = tmem + t_lane + kDeferA0 + g * kDeferAStride;
     const uint32_t p_addr = tmem + t_lane + g * NT;
@@ -380,7 +389,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         const uint8_t* st = wring + cs * WST;
         const float scale = scale_to_f32<SCL>(reinterpret_cast<const uint16_t*>(st + S_OFF)[si]);
         uint32_t zero = 1u << (BITS - 1);
-        if (a.has_zeros) zero = (reinterpret_cast<const uint32_t*>(st + Z_OFF)[zi] >> zshift) & ZMASK;
+        if (a.has_zeros) zero = (reinterpret_cast<const uint32_t*>(st + z_off)[zi] >> zshift) & ZMASK;
         // codes of this row -> A slot g (magic-number form)
         const uint4* src = row_base + cs * (WST / 16);
 #pragma unroll

@@ -298,10 +298,12 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_s);
+    if (!a.wpack) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_s);
+      if (a.has_zeros) prefetch_tmap(&tm_z);
+    }
     prefetch_tmap(&tm_b);
-    if (a.has_zeros) prefetch_tmap(&tm_z);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, a.tmem_cols);
@@ -323,7 +325,8 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     // 64-wide K chunks of the token tile: five copies for 8-16 KB of codes.
     // The whole warp runs the loop (waits are warp-wide polls); one elected
     // lane issues the copies.
-    const uint32_t stage_tx = W_BYTES + SG * 256 + (a.has_zeros ? SG * (kTileRows / PF) * 4 : 0) + BST;
+    const uint32_t stage_tx =
+        (a.wpack ? a.wimg : W_BYTES + SG * 256 + (a.has_zeros ? SG * (kTileRows / PF) * 4 : 0)) + BST;
     const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
     const uint64_t pol_b = l2_policy_evict_last();   // token rows: re-read by every row tile
     int it = 0, s = 0;
@@ -338,7 +341,12 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
           mbar_arrive_expect_tx(&full[s], stage_tx);
           uint8_t* dst = wring + s * WST;
           const int ys = e * a.groups + (kt * kTileK) / a.G;
-          if (GEMM == 1) {
+          if (a.wpack) {
+            // prepacked: the stage's codes, scales and zero points as one image
+            const uint8_t* src =
+                a.wpack + ((static_cast<size_t>(e) * a.n_tiles + w.tile) * a.kt_total + kt) * a.wimg;
+            bulk_load(dst, src, a.wimg, &full[s], pol_w);
+          } else if (GEMM == 1) {
             const int f0 = w.tile * kGateUpRows;
             tma_load_3d(dst, &tm_q, &full[s], kt * KW, f0, 2 * e, pol_w);
             tma_load_3d(dst + S_OFF, &tm_s, &full[s], f0, 0, ys, pol_w);
@@ -450,6 +458,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
       hrow = srow;
     }
     const uint32_t t_lane = (q * 32) << 16;
+    const int z_off = a.wpack ? W_BYTES + SG * 256 : Z_OFF;  // zero points: right after the scales in an image
     // This group's stages are the running stage indices gi = grp, grp + step,
     // ... across units (step 2, or 1 for LEAN). Tracked incrementally: the ring
     // slot cs and phase cf of stage gi, its A slot cslot, and the ring slot cps
@@ -484,7 +493,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
           if (a.has_zeros) {
             const int zi = GEMM == 1 ? (gr * 2 + half) * (kGateUpRows / PF) + hrow / PF
                                      : gr * (kTileRows / PF) + hrow / PF;
-            zero[c] = (reinterpret_cast<const uint32_t*>(st + Z_OFF)[zi] >> (BITS * (hrow % PF))) & ZMASK;
+            zero[c] = (reinterpret_cast<const uint32_t*>(st + z_off)[zi] >> (BITS * (hrow % PF))) & ZMASK;
           }
         }
         // Code rows are TMA-swizzled (64-byte rows: 16-byte chunk c of row r sits at

@@ -379,24 +379,34 @@ size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, i
   return ws_layout(M, H, I, E, topk, r.block, r.split, r.split1).total;
 }
 
-wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
-                                   int64_t I, int E, int topk, const int32_t* w13_q,
-                                   const void* w13_scales, const int32_t* w13_zeros, const int32_t* w2_q,
-                                   const void* w2_scales, const int32_t* w2_zeros,
-                                   wna16_dtype scale_dtype, int bits, int group_size,
-                                   const int32_t* topk_ids, const float* topk_weights, void* out,
-                                   void* workspace, size_t workspace_bytes, int block, int split_k,
-                                   void* stream, void* const* events) {
+}  // extern "C"
+
+namespace {
+
+// The fused layer on either weight form: the plain layout (w13_q, ...,
+// w2_zeros, read by TMA boxes) or prepacked stage images (w13_pack, w2_pack,
+// one bulk copy per stage; the plain pointers are then unused).
+wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I, int E,
+                       int topk, const int32_t* w13_q, const void* w13_scales, const int32_t* w13_zeros,
+                       const int32_t* w2_q, const void* w2_scales, const int32_t* w2_zeros,
+                       const void* w13_pack, const void* w2_pack, int pack_zeros, wna16_dtype scale_dtype,
+                       int bits, int group_size, const int32_t* topk_ids, const float* topk_weights, void* out,
+                       void* workspace, size_t workspace_bytes, int block, int split_k, void* stream,
+                       void* const* events) {
   if (act_dtype != WNA16_F16 && act_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
   if (scale_dtype != WNA16_F16 && scale_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
   Resolved r;
   const wna16_status st = resolve(M, H, I, E, topk, bits, group_size, block, split_k, &r);
   if (st != WNA16_OK) return st;
   if (M == 0) return WNA16_OK;
-  if (!hidden || !w13_q || !w13_scales || !w2_q || !w2_scales || !topk_ids || !topk_weights || !out ||
-      !workspace)
-    return WNA16_ERR_INVALID_ARG;
-  if ((w13_zeros == nullptr) != (w2_zeros == nullptr)) return WNA16_ERR_INVALID_ARG;
+  const bool packed = w13_pack != nullptr || w2_pack != nullptr;
+  if (!hidden || !topk_ids || !topk_weights || !out || !workspace) return WNA16_ERR_INVALID_ARG;
+  if (packed) {
+    if (!w13_pack || !w2_pack || !aligned16(w13_pack) || !aligned16(w2_pack)) return WNA16_ERR_INVALID_ARG;
+  } else {
+    if (!w13_q || !w13_scales || !w2_q || !w2_scales) return WNA16_ERR_INVALID_ARG;
+    if ((w13_zeros == nullptr) != (w2_zeros == nullptr)) return WNA16_ERR_INVALID_ARG;
+  }
   const void* ptrs[] = {hidden, w13_q, w13_scales, w13_zeros, w2_q, w2_scales, w2_zeros, out, workspace};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return WNA16_ERR_INVALID_ARG;
@@ -421,7 +431,7 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   const int B = r.block;
   const int64_t cap = capacity(P, E, B);
   const int max_blocks = static_cast<int>(cap / B);
-  const bool zeros = w13_zeros != nullptr;
+  const bool zeros = packed ? pack_zeros != 0 : w13_zeros != nullptr;
   // 16- and 32-token tiles run the deferred-scale kernel when every stage lies
   // in one group (G >= 128) and the code/activation formats have a
   // magic-number form.
@@ -436,8 +446,11 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
     return true;
   };
   GemmMaps m1, m2;
-  if (!make_gemm_maps(&m1, w13_q, w13_scales, zeros ? w13_zeros : nullptr, E, 2 * I, H, r.G1, bits, true) ||
-      !make_gemm_maps(&m2, w2_q, w2_scales, zeros ? w2_zeros : nullptr, E, H, I, r.G2, bits, false))
+  std::memset(&m1, 0, sizeof(m1));
+  std::memset(&m2, 0, sizeof(m2));
+  if (!packed &&
+      (!make_gemm_maps(&m1, w13_q, w13_scales, zeros ? w13_zeros : nullptr, E, 2 * I, H, r.G1, bits, true) ||
+       !make_gemm_maps(&m2, w2_q, w2_scales, zeros ? w2_zeros : nullptr, E, H, I, r.G2, bits, false)))
     return WNA16_ERR_CUDA;
   // Token tiles: `block` expert-sorted rows of 64 elements per stage, in the
   // 128-byte swizzled K-major layout (gathered hidden rows; the act cache).
@@ -506,6 +519,8 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a1.cap = static_cast<int>(cap);
   a1.part = part1;
   a1.counters = cnt1;
+  a1.wpack = packed ? static_cast<const uint8_t*>(w13_pack) : nullptr;
+  a1.wimg = prepack_image_bytes(bits, prepack_sg(r.G1), zeros ? 1 : 0);
   const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles * split1;
   const int64_t slots = static_cast<int64_t>(sms) * pipe.ctas_per_sm;
   const dim3 grid1(static_cast<unsigned>(std::min<int64_t>(units1, slots)));
@@ -528,6 +543,8 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
   a2.n_tiles = static_cast<int>((H + kTileRows - 1) / kTileRows);
   a2.groups = static_cast<int>(I / r.G2);
   a2.panel = panel_blocks(B, I, max_blocks);
+  a2.wpack = packed ? static_cast<const uint8_t*>(w2_pack) : nullptr;
+  a2.wimg = prepack_image_bytes(bits, prepack_sg(r.G2), zeros ? 1 : 0);
   a2.G = r.G2;
   a2.kt_total = static_cast<int>((I + kTileK - 1) / kTileK);
   a2.split = r.split;
@@ -549,6 +566,35 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
     return WNA16_ERR_CUDA;
   if (!mark(5)) return WNA16_ERR_CUDA;
   return WNA16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
+                                   int64_t I, int E, int topk, const int32_t* w13_q,
+                                   const void* w13_scales, const int32_t* w13_zeros, const int32_t* w2_q,
+                                   const void* w2_scales, const int32_t* w2_zeros,
+                                   wna16_dtype scale_dtype, int bits, int group_size,
+                                   const int32_t* topk_ids, const float* topk_weights, void* out,
+                                   void* workspace, size_t workspace_bytes, int block, int split_k,
+                                   void* stream, void* const* events) {
+  return run_layer(hidden, act_dtype, M, H, I, E, topk, w13_q, w13_scales, w13_zeros, w2_q, w2_scales, w2_zeros,
+                   nullptr, nullptr, 0, scale_dtype, bits, group_size, topk_ids, topk_weights, out, workspace,
+                   workspace_bytes, block, split_k, stream, events);
+}
+
+wna16_status wna16_fused_moe_prepacked(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
+                                       int64_t I, int E, int topk, const void* w13_packed, const void* w2_packed,
+                                       int has_zeros, wna16_dtype scale_dtype, int bits, int group_size,
+                                       const int32_t* topk_ids, const float* topk_weights, void* out,
+                                       void* workspace, size_t workspace_bytes, int block, int split_k,
+                                       void* stream, void* const* events) {
+  if (!w13_packed || !w2_packed) return WNA16_ERR_INVALID_ARG;
+  return run_layer(hidden, act_dtype, M, H, I, E, topk, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                   w13_packed, w2_packed, has_zeros, scale_dtype, bits, group_size, topk_ids, topk_weights, out,
+                   workspace, workspace_bytes, block, split_k, stream, events);
 }
 
 wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I,
