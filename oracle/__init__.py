@@ -13,6 +13,9 @@ from .wna16_oracle import (  # noqa: F401
     dequantize_expert,
     align_capacity,
     moe_align_block_size,
+    routing_scores,
+    routing_group_scores,
+    topk_routing,
     silu,
     fused_moe_per_token,
     fused_moe_grouped,

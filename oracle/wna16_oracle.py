@@ -184,6 +184,99 @@ def moe_align_block_size(topk_ids: np.ndarray, E: int, block: int):
 
 
 # ----------------------------------------------------------------------------
+# routing: router logits -> top-k expert ids and weights
+# ----------------------------------------------------------------------------
+#
+# The pages name top-k routing ids and weights as the first stage of the layer
+# (the Mixtral, Qwen2-MoE and DeepSeek-V3 models of vLLM PR #12185 and PR #6502)
+# but give no formulas. Stated readings:
+# * softmax scores p_e = exp(l_e) / sum_e' exp(l_e'); sigmoid scores
+#   s_e = 1 / (1 + exp(-l_e));
+# * experts are ranked by logit, larger first, ties to the lower index, NaN
+#   ranked as -inf (both score functions are increasing in the logit, so
+#   this is the ranking by score, decided on the exact inputs);
+# * grouped selection (DeepSeek-V3 style): experts split into n_groups equal
+#   groups of consecutive ids; a group's score is the sum of the scores of its
+#   two best-ranked experts; the topk_groups best groups are kept (larger score
+#   first, ties to the lower group); the top-k experts are ranked among the
+#   kept groups only;
+# * weights: the selected scores, or with ``renormalize`` the selected scores
+#   divided by their sum (for softmax, the softmax over the selected logits);
+# * output slot j holds the j-th best selected expert.
+
+
+def _rank_order(logits_row, allowed=None):
+    """Expert indices, best first: larger logit, then lower index; NaN as -inf."""
+    idx = range(len(logits_row)) if allowed is None else allowed
+
+    def key(e):
+        v = float(logits_row[e])
+        return (math.inf if math.isnan(v) else -v, e)
+
+    return sorted(idx, key=key)
+
+
+def routing_scores(logits: np.ndarray, scoring: str) -> np.ndarray:
+    """Softmax (over all experts of a row) or sigmoid scores, float64."""
+    l = np.asarray(logits, dtype=np.float64)
+    if scoring == "softmax":
+        m = np.max(l, axis=-1, keepdims=True)
+        ex = np.exp(l - m)
+        return ex / np.sum(ex, axis=-1, keepdims=True)
+    if scoring == "sigmoid":
+        return 1.0 / (1.0 + np.exp(-l))
+    raise ValueError(scoring)
+
+
+def routing_group_scores(logits: np.ndarray, scoring: str, n_groups: int) -> np.ndarray:
+    """[M, n_groups]: sum of the scores of the two best-ranked experts of each group."""
+    l = np.asarray(logits, dtype=np.float64)
+    M, E = l.shape
+    gs = E // n_groups
+    sc = routing_scores(l, scoring)
+    out = np.zeros((M, n_groups), dtype=np.float64)
+    for t in range(M):
+        for g in range(n_groups):
+            members = list(range(g * gs, (g + 1) * gs))
+            best2 = _rank_order(l[t], members)[:2]
+            out[t, g] = sc[t, best2[0]] + sc[t, best2[1]]
+    return out
+
+
+def topk_routing(logits: np.ndarray, topk: int, scoring: str = "softmax", renormalize: bool = True,
+                 n_groups: int = 1, topk_groups: int = 1):
+    """Router logits [M, E] -> (topk_ids [M, topk] int32, topk_weights [M, topk] float64).
+
+    See the readings above. ``n_groups == 1`` is plain top-k; with
+    ``n_groups > 1`` the group size E / n_groups must be at least 2.
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    M, E = l.shape
+    if not (1 <= topk <= E) or E % n_groups:
+        raise ValueError("bad routing shape")
+    sc = routing_scores(l, scoring)
+    gsc = routing_group_scores(l, scoring, n_groups) if n_groups > 1 else None
+    gs = E // n_groups
+    ids = np.zeros((M, topk), dtype=np.int32)
+    w = np.zeros((M, topk), dtype=np.float64)
+    for t in range(M):
+        allowed = None
+        if n_groups > 1:
+            kept = sorted(range(n_groups), key=lambda g: (-gsc[t, g], g))[:topk_groups]
+            allowed = [e for g in sorted(kept) for e in range(g * gs, (g + 1) * gs)]
+        sel = _rank_order(l[t], allowed)[:topk]
+        ids[t] = sel
+        if renormalize and scoring == "softmax":
+            ex = np.exp(l[t, sel] - l[t, sel[0]])
+            w[t] = ex / ex.sum()
+        elif renormalize:
+            w[t] = sc[t, sel] / sc[t, sel].sum()
+        else:
+            w[t] = sc[t, sel]
+    return ids, w
+
+
+# ----------------------------------------------------------------------------
 # the layer
 # ----------------------------------------------------------------------------
 

@@ -114,6 +114,29 @@ def _gen(seed: int, device) -> torch.Generator:
 # routing (inputs of the layer: top-k expert ids and weights)
 # ----------------------------------------------------------------------------
 
+def make_router_logits(wl: Workload, M: int, seed: int) -> torch.Tensor:
+    """Router logits [M, E] float32 on CPU: N(0, 1), plus log p_rank(e) for the
+    Zipf-skewed workloads (p_r ~ r^-s over a seeded rank permutation)."""
+    g = _gen(seed, "cpu")
+    logits = torch.randn(M, wl.E, generator=g, dtype=torch.float64)
+    if wl.zipf_s is not None:
+        rank = torch.randperm(wl.E, generator=_gen(_seed(wl.name, "zipf"), "cpu")) + 1
+        p = rank.double() ** (-wl.zipf_s)
+        logits = logits + torch.log(p / p.sum())[None, :]
+    return logits.float().contiguous()
+
+
+def routing_params(wl: Workload) -> dict:
+    """The workload's routing as keyword arguments of the routing call."""
+    if wl.routing == "softmax_renorm":
+        return dict(scoring="softmax", renormalize=True, n_groups=1, topk_groups=1)
+    if wl.routing == "softmax":
+        return dict(scoring="softmax", renormalize=False, n_groups=1, topk_groups=1)
+    if wl.routing == "sigmoid_grouped":
+        return dict(scoring="sigmoid", renormalize=True, n_groups=wl.n_groups, topk_groups=wl.topk_groups)
+    raise ValueError(wl.routing)
+
+
 def make_routing(wl: Workload, M: int, seed: int):
     """Router logits -> (topk_ids [M,k] int32, topk_weights [M,k] fp32), on CPU.
 
@@ -125,12 +148,7 @@ def make_routing(wl: Workload, M: int, seed: int):
     Zipf skew (Qwen2 workload): logits += log p_rank(e), p_r ~ r^-s with a seeded
     rank permutation, so a few experts get most tokens.
     """
-    g = _gen(seed, "cpu")
-    logits = torch.randn(M, wl.E, generator=g, dtype=torch.float64)
-    if wl.zipf_s is not None:
-        rank = torch.randperm(wl.E, generator=_gen(_seed(wl.name, "zipf"), "cpu")) + 1
-        p = rank.double() ** (-wl.zipf_s)
-        logits = logits + torch.log(p / p.sum())[None, :]
+    logits = make_router_logits(wl, M, seed).double()
     if wl.routing == "softmax_renorm":
         top, ids = torch.topk(logits, wl.topk, dim=-1)
         w = torch.softmax(top, dim=-1)
