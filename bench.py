@@ -455,6 +455,7 @@ def ours_arm(args):
                           "kernels_us": [float(v) * 1e3 for v in perx.mean(axis=0)]})
             del lix, callx
         line["sweep"] = sweep
+        line["routing"] = routing_times(w, wl, dev, flush, sorted({M, max(wl.m_sweep), 8192}), peaks)
     if rank == 0 and not args.no_cpu_baseline:
         rate, desc, secs = time_oracle(li, 10.0)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
@@ -465,6 +466,33 @@ def ours_arm(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def routing_times(w, wl, dev, flush, Ms, peaks, steps=40):
+    """The routing kernel (router logits -> top-k ids and weights) on the
+    workload's fp32 logits, L2 flushed before each launch. Not part of the step:
+    the layer takes ids and weights as inputs."""
+    from synthetic import make_router_logits, routing_params
+
+    out = []
+    for Mx in Ms:
+        x = make_router_logits(wl, Mx, 4242 + Mx).to(dev)
+        ids = torch.empty(Mx, wl.topk, dtype=torch.int32, device=dev)
+        wt = torch.empty(Mx, wl.topk, dtype=torch.float32, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(3 + steps):
+            flush.zero_()
+            if i >= 3:
+                evs[i - 3][0].record()
+            w.topk_routing(x, wl.topk, topk_ids=ids, topk_weights=wt, **routing_params(wl))
+            if i >= 3:
+                evs[i - 3][1].record()
+        torch.cuda.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        nbytes = Mx * wl.E * 4 + Mx * wl.topk * 8
+        out.append({"M": Mx, "us": ms * 1e3, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
+                    "hbm_frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]})
+    return out
 
 
 def e2e(w, wl, li, ws, flush, dev, steps):

@@ -69,7 +69,12 @@ typedef enum {
   WNA16_ERR_DEVICE_TIMEOUT = 6        /* device: a pipeline wait gave up */
 } wna16_status;
 
-typedef enum { WNA16_F16 = 0, WNA16_BF16 = 1 } wna16_dtype;
+/* Element types. Activations, outputs and scales: F16 or BF16; F32 only for
+ * router logits (wna16_topk_routing). */
+typedef enum { WNA16_F16 = 0, WNA16_BF16 = 1, WNA16_F32 = 2 } wna16_dtype;
+
+/* Router score functions of wna16_topk_routing. */
+typedef enum { WNA16_SCORE_SOFTMAX = 0, WNA16_SCORE_SIGMOID = 1 } wna16_scoring;
 
 /* Device status bits (the int32 at offset 0 of the fused-call workspace). */
 #define WNA16_DEV_BAD_EXPERT_ID 0x1
@@ -110,6 +115,38 @@ wna16_status wna16_moe_align_block_size(const int32_t* topk_ids, int64_t M, int 
  * [16, 256] closest to the expected pairs per active expert.
  */
 int wna16_choose_block(int64_t M, int topk, int E);
+
+/*
+ * Top-k routing: router logits -> the topk_ids / topk_weights the align and
+ * fused calls take. The pages name top-k routing ids and weights as the
+ * layer's first stage (vLLM PR #12185; the Mixtral, Qwen2-MoE and DeepSeek-V3
+ * models of PR #12185 and PR #6502) and give no formulas; these are the
+ * readings implemented:
+ *   scores: softmax over the row's E logits, or sigmoid 1 / (1 + exp(-l));
+ *   ranking: larger logit first, ties to the lower expert index, NaN ranked as
+ *     -inf (both score functions increase with the logit, so this is the
+ *     ranking by score, taken on the exact input values);
+ *   n_groups > 1 (DeepSeek-V3 style): experts [g*E/n_groups, (g+1)*E/n_groups)
+ *     form group g; a group's score is the sum of the scores of its two
+ *     best-ranked experts (fp32); the topk_groups best groups are kept (larger
+ *     score first, ties to the lower group, NaN as -inf) and the top-k experts
+ *     are ranked among them only;
+ *   weights: the selected scores; with renormalize != 0 divided by their sum
+ *     (for softmax: the softmax over the selected logits). Computed in fp32.
+ *   logits       [M, E] fp32, fp16 or bf16 (logits_dtype), row-major, aligned
+ *                to its element size.
+ *   topk_ids     [M, topk] int32 out: slot j = the j-th best selected expert.
+ *   topk_weights [M, topk] fp32 out.
+ *   E in [1, 256], topk in [1, min(E, 32)], n_groups in [1, 32] dividing E;
+ *   with n_groups > 1: E / n_groups >= 2, topk_groups in [1, n_groups] and
+ *   topk <= topk_groups * E / n_groups (topk_groups is ignored otherwise).
+ * One warp per row, one launch, no workspace, graph-safe. M = 0 launches
+ * nothing. Non-finite logits give valid, distinct ids; their weights follow
+ * IEEE arithmetic (NaN may appear).
+ */
+wna16_status wna16_topk_routing(const void* logits, wna16_dtype logits_dtype, int64_t M, int E, int topk,
+                                wna16_scoring scoring, int renormalize, int n_groups, int topk_groups,
+                                int32_t* topk_ids, float* topk_weights, void* stream);
 
 /*
  * Bytes of workspace wna16_fused_moe needs for these sizes on the current

@@ -198,8 +198,8 @@ def moe_align_block_size(topk_ids: np.ndarray, E: int, block: int):
 # * grouped selection (DeepSeek-V3 style): experts split into n_groups equal
 #   groups of consecutive ids; a group's score is the sum of the scores of its
 #   two best-ranked experts; the topk_groups best groups are kept (larger score
-#   first, ties to the lower group); the top-k experts are ranked among the
-#   kept groups only;
+#   first, ties to the lower group, NaN as -inf); the top-k experts are ranked
+#   among the kept groups only;
 # * weights: the selected scores, or with ``renormalize`` the selected scores
 #   divided by their sum (for softmax, the softmax over the selected logits);
 # * output slot j holds the j-th best selected expert.
@@ -262,7 +262,8 @@ def topk_routing(logits: np.ndarray, topk: int, scoring: str = "softmax", renorm
     for t in range(M):
         allowed = None
         if n_groups > 1:
-            kept = sorted(range(n_groups), key=lambda g: (-gsc[t, g], g))[:topk_groups]
+            kept = sorted(range(n_groups),
+                          key=lambda g: (math.inf if math.isnan(gsc[t, g]) else -gsc[t, g], g))[:topk_groups]
             allowed = [e for g in sorted(kept) for e in range(g * gs, (g + 1) * gs)]
         sel = _rank_order(l[t], allowed)[:topk]
         ids[t] = sel

@@ -88,6 +88,8 @@ def test_fused_argument_errors_are_host_side(lib):
     assert _call_fused(lib, block=48) == 1
     assert _call_fused(lib, block=512) == 1
     assert _call_fused(lib, split=9) == 1
+    assert _call_fused(lib, split=-1) == 1
+    assert _call_fused(lib, act=2) == 1  # fp32 is for router logits only
     assert _call_fused(lib, w13_z=16) == 1  # zeros for one projection only
     assert _call_fused(lib, act=5) == 1
     assert _call_fused(lib, ws_bytes=16) == 3
@@ -100,3 +102,31 @@ def test_workspace_bytes_cover_the_layout(lib):
     cap = oracle.align_capacity(P, 256, B)
     assert n >= cap * 4 + cap * 2048 * 2 + P * 7168 * 4
     assert lib.wna16_fused_moe_workspace_bytes(4, 256, 512, 8, 2, 3, 128, 0, 0) == 0
+
+
+def _call_routing(lib, **over):
+    a = dict(logits=16, dt=2, M=4, E=256, k=8, scoring=1, renorm=1, ng=8, tg=4, ids=16, w=16)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return lib.wna16_topk_routing(vp(a["logits"]) if a["logits"] else None, a["dt"], a["M"], a["E"], a["k"],
+                                  a["scoring"], a["renorm"], a["ng"], a["tg"],
+                                  vp(a["ids"]) if a["ids"] else None, vp(a["w"]) if a["w"] else None, None)
+
+
+def test_routing_argument_errors_are_host_side(lib):
+    assert _call_routing(lib, M=0) == 0  # nothing launched
+    assert _call_routing(lib, logits=None) == 1
+    assert _call_routing(lib, logits=18) == 1  # fp32 logits need 4-byte alignment
+    assert _call_routing(lib, ids=None) == 1
+    assert _call_routing(lib, E=257) == 1
+    assert _call_routing(lib, k=33) == 1
+    assert _call_routing(lib, E=4, k=5, ng=1) == 1  # topk > E
+    assert _call_routing(lib, ng=7) == 1  # groups must divide E
+    assert _call_routing(lib, ng=64, E=256) == 1  # at most 32 groups
+    assert _call_routing(lib, ng=4, E=4, k=1, tg=1) == 1  # groups of one expert
+    assert _call_routing(lib, tg=9) == 1
+    assert _call_routing(lib, tg=0) == 1
+    assert _call_routing(lib, k=9, E=32, ng=8, tg=2) == 1  # only 8 experts kept
+    assert _call_routing(lib, scoring=2) == 1
+    assert _call_routing(lib, dt=3) == 1
+

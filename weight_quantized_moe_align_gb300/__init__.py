@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     moe_align_block_size,
     prepack,
     read_device_status,
+    topk_routing,
     workspace_bytes,
 )
 from .build import LIB, build  # noqa: F401

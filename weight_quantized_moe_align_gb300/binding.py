@@ -31,10 +31,12 @@ EXPORTED = (
     "wna16_align_capacity", "wna16_moe_align_block_size", "wna16_choose_block",
     "wna16_fused_moe_workspace_bytes", "wna16_fused_moe", "wna16_fused_moe_timed",
     "wna16_fused_moe_noalloc", "wna16_prepack_bytes", "wna16_prepack", "wna16_fused_moe_prepacked",
-    "wna16_read_device_status", "wna16_status_string",
+    "wna16_read_device_status", "wna16_status_string", "wna16_topk_routing",
 )
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
+_LOGIT_DTYPE = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
+_SCORING = {"softmax": 0, "sigmoid": 1}
 
 
 class WNA16Error(RuntimeError):
@@ -81,6 +83,8 @@ def load() -> ctypes.CDLL:
     L.wna16_fused_moe_prepacked.restype = i32
     L.wna16_read_device_status.argtypes = [vp, c.POINTER(c.c_int32), vp]
     L.wna16_read_device_status.restype = i32
+    L.wna16_topk_routing.argtypes = [vp, i32, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    L.wna16_topk_routing.restype = i32
     L.wna16_status_string.argtypes = [i32]
     L.wna16_status_string.restype = c.c_char_p
     _lib = L
@@ -130,6 +134,31 @@ def workspace_bytes(M, H, I, E, topk, bits, group_size, block=0, split_k=0) -> i
     if n == 0 and M > 0:
         raise WNA16Error(1, "wna16_fused_moe_workspace_bytes")
     return n
+
+
+def topk_routing(logits: torch.Tensor, topk: int, scoring: str = "softmax", renormalize: bool = True,
+                 n_groups: int = 1, topk_groups: int = 1, topk_ids: Optional[torch.Tensor] = None,
+                 topk_weights: Optional[torch.Tensor] = None, stream=None):
+    """Router logits [M, E] (fp32/fp16/bf16) -> (topk_ids [M, topk] int32,
+    topk_weights [M, topk] fp32) by ``wna16_topk_routing``."""
+    _check(logits, "logits", tuple(_LOGIT_DTYPE))
+    if logits.dim() != 2:
+        raise ValueError("logits must be [M, E]")
+    if scoring not in _SCORING:
+        raise ValueError(f"scoring must be one of {tuple(_SCORING)}")
+    M, E = logits.shape
+    dev = logits.device
+    if topk_ids is None:
+        topk_ids = torch.empty(M, topk, dtype=torch.int32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty(M, topk, dtype=torch.float32, device=dev)
+    _check(topk_ids, "topk_ids", torch.int32, (M, topk), dev)
+    _check(topk_weights, "topk_weights", torch.float32, (M, topk), dev)
+    st = load().wna16_topk_routing(_ptr(logits), _LOGIT_DTYPE[logits.dtype], M, E, topk, _SCORING[scoring],
+                                   int(bool(renormalize)), n_groups, topk_groups, _ptr(topk_ids),
+                                   _ptr(topk_weights), _stream(stream))
+    _raise(st, "wna16_topk_routing")
+    return topk_ids, topk_weights
 
 
 def moe_align_block_size(topk_ids: torch.Tensor, E: int, block: int, with_counts=True,
