@@ -17,6 +17,7 @@ from .wna16_oracle import (  # noqa: F401
     routing_group_scores,
     topk_routing,
     silu,
+    gated_activation,
     fused_moe_per_token,
     fused_moe_grouped,
 )

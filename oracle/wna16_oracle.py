@@ -286,6 +286,32 @@ def silu(v: np.ndarray) -> np.ndarray:
     return v / (1.0 + np.exp(-v))
 
 
+def gated_activation(g: np.ndarray, u: np.ndarray, glu=None) -> np.ndarray:
+    """The gate/up activation.
+
+    ``glu`` None: silu(g) * u. ``glu = (alpha, beta, limit)`` (the clamped SwiGLU
+    that vLLM's int8 MoE config passes as swiglu_alpha / swiglu_beta /
+    swiglu_limit, with no formula on the pages; the reading taken): with
+    limit > 0, g' = min(g, limit) and u' = clamp(u, -limit, limit), else g' = g,
+    u' = u; result g' * sigmoid(alpha * g') * (u' + beta). alpha = 1, beta = 0
+    and no limit give silu(g) * u.
+    """
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    if glu is None:
+        return silu(g) * u
+    alpha, beta, limit = (float(v) for v in glu)
+    if limit > 0:
+        g = np.minimum(g, limit)
+        u = np.clip(u, -limit, limit)
+    return g / (1.0 + np.exp(-alpha * g)) * (u + beta)
+
+
+def _bias(L, key, e, dtype):
+    b = L.get(key)
+    return None if b is None else halfbits_to_f64(b[e], dtype)
+
+
 def _expert_matrices(L, e, cache):
     if e not in cache:
         w13 = dequantize_expert(L["w13_q"][e], L["w13_s"][e],
@@ -305,10 +331,13 @@ def fused_moe_per_token(L: dict, tokens=None, round_output=True):
     ``w13_s`` [E, H/G, 2I] raw bits, ``w13_z`` [E, H/G, 2I/pf] or None, ``w2_q``
     [E, H, I/pf], ``w2_s`` [E, I/G, H], ``w2_z`` [E, I/G, H/pf] or None,
     ``scale_dtype``, ``bits``, ``group_size``, ``topk_ids`` [M, k], ``topk_w`` [M, k]
-    float32. For each token t and slot j with expert e = ids[t, j] in [0, E):
-    g = W13[e, :I] x_t, u = W13[e, I:] x_t, a = silu(g) * u, y = W2[e] a;
-    out_t = sum_j w[t, j] y_{t,j} in slot order. Returns float64 [T, H], or the
-    raw half bits of its single rounding when ``round_output``.
+    float32; optional ``w13_b`` [E, 2I] / ``w2_b`` [E, H] raw half bits of the
+    activation dtype (biases) and ``glu`` (see :func:`gated_activation`). For each
+    token t and slot j with expert e = ids[t, j] in [0, E):
+    g = W13[e, :I] x_t + b13[e, :I], u = W13[e, I:] x_t + b13[e, I:],
+    a = act(g, u), y = W2[e] a + b2[e]; out_t = sum_j w[t, j] y_{t,j} in slot
+    order. Returns float64 [T, H], or the raw half bits of its single rounding
+    when ``round_output``.
     """
     x = halfbits_to_f64(L["x"], L["act_dtype"])
     ids = np.asarray(L["topk_ids"])
@@ -328,8 +357,15 @@ def fused_moe_per_token(L: dict, tokens=None, round_output=True):
                 continue
             w13, w2 = _expert_matrices(L, e, cache)
             gu = w13 @ x[t]
-            a = silu(gu[:I]) * gu[I:]
-            acc = acc + tw[t, j] * (w2 @ a)
+            b13 = _bias(L, "w13_b", e, L["act_dtype"])
+            if b13 is not None:
+                gu = gu + b13
+            a = gated_activation(gu[:I], gu[I:], L.get("glu"))
+            y = w2 @ a
+            b2 = _bias(L, "w2_b", e, L["act_dtype"])
+            if b2 is not None:
+                y = y + b2
+            acc = acc + tw[t, j] * y
         rows.append(acc)
     out = np.stack(rows) if rows else np.zeros((0, H))
     return round_to_halfbits(out, L["act_dtype"]) if round_output else out
@@ -354,8 +390,15 @@ def fused_moe_grouped(L: dict, round_output=True):
             continue
         w13, w2 = _expert_matrices(L, e, {})
         gu = x[tt] @ w13.T
-        a = silu(gu[:, :I]) * gu[:, I:]
-        y[tt, jj] = (a @ w2.T) * tw[tt, jj][:, None]
+        b13 = _bias(L, "w13_b", e, L["act_dtype"])
+        if b13 is not None:
+            gu = gu + b13[None, :]
+        a = gated_activation(gu[:, :I], gu[:, I:], L.get("glu"))
+        ye = a @ w2.T
+        b2 = _bias(L, "w2_b", e, L["act_dtype"])
+        if b2 is not None:
+            ye = ye + b2[None, :]
+        y[tt, jj] = ye * tw[tt, jj][:, None]
     out = np.zeros((M, H), dtype=np.float64)
     for j in range(k):
         out = out + y[:, j]

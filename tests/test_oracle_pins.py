@@ -386,3 +386,93 @@ def test_tiny_workload_oracle_forms_agree():
     fa = oracle.halfbits_to_f64(a, "f16")
     fb = oracle.halfbits_to_f64(b, "f16")
     assert np.max(np.abs(fa - fb)) <= np.max(np.abs(fa)) * 2.0 ** -10
+
+
+# ----------------------------------------------------------------------------
+# biases and the clamped SwiGLU (vLLM int8 MoE config: w1_bias / w2_bias,
+# swiglu_alpha / swiglu_beta / swiglu_limit; readings in the oracle)
+# ----------------------------------------------------------------------------
+
+def test_gated_activation_closed_forms():
+    sig = lambda v: 1.0 / (1.0 + math.exp(-v))
+    act = lambda g, u, glu=None: float(oracle.gated_activation(np.array([g]), np.array([u]), glu)[0])
+    assert act(1.0, 2.0) == pytest.approx(2.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+    # gate clamped from above only, up from both sides, beta added after the clamp:
+    # (9, -8) -> (7, -7): 7 * sigmoid(2 * 7) * (-7 + 1)
+    assert act(9.0, -8.0, (2.0, 1.0, 7.0)) == pytest.approx(-42.0 * sig(14.0), rel=1e-15)
+    # (-9, 9) -> (-9, 7): -9 * sigmoid(-18) * 8
+    assert act(-9.0, 9.0, (2.0, 1.0, 7.0)) == pytest.approx(-72.0 * sig(-18.0), rel=1e-15)
+    # inside the limit nothing is clamped
+    assert act(3.0, 0.5, (2.0, 1.0, 7.0)) == pytest.approx(3.0 * sig(6.0) * 1.5, rel=1e-15)
+    # limit <= 0: no clamp
+    assert act(9.0, -8.0, (2.0, 1.0, 0.0)) == pytest.approx(9.0 * sig(18.0) * -7.0, rel=1e-15)
+    # alpha = 1, beta = 0, no limit is silu(g) * u
+    rng = np.random.default_rng(3)
+    g, u = rng.standard_normal(50) * 4, rng.standard_normal(50) * 4
+    np.testing.assert_allclose(oracle.gated_activation(g, u, (1.0, 0.0, 0.0)), oracle.gated_activation(g, u),
+                               rtol=1e-15)
+
+
+def _half(v, dt="f16"):
+    return halfbits(torch.as_tensor(np.asarray(v, dtype=np.float32)).to(
+        torch.float16 if dt == "f16" else torch.bfloat16))
+
+
+def test_layer_biases_closed_form_zero_weights():
+    # all codes at the zero point: W13 = W2 = 0, so y = b2[e] for every slot and
+    # out_t = sum_j w_tj b2[e_tj], whatever b13 and the activation are
+    L = _small_layer(has_zeros=False)
+    E, H, I = 4, 64, 32
+    L["w13_q"] = pack_along_last(torch.full((E, 2 * I, H), 8), 4).numpy()
+    L["w2_q"] = pack_along_last(torch.full((E, H, I), 8), 4).numpy()
+    rng = np.random.default_rng(1)
+    b2 = rng.standard_normal((E, H))
+    L["w13_b"] = _half(rng.standard_normal((E, 2 * I)) * 4)
+    L["w2_b"] = _half(b2)
+    b2 = oracle.halfbits_to_f64(L["w2_b"], "f16")
+    tw = L["topk_w"].astype(np.float64)
+    want = sum(tw[:, j, None] * b2[L["topk_ids"][:, j]] for j in range(2))
+    for glu in (None, (1.702, 1.0, 7.0)):
+        got = oracle.fused_moe_per_token(dict(L, glu=glu), round_output=False)
+        np.testing.assert_allclose(got, want, rtol=1e-14, atol=1e-15)
+
+
+def test_layer_biases_closed_form_constant_down():
+    # W13 = 0 and every down weight b: g_i = b13[e, i], u_i = b13[e, I + i],
+    # y_h = b * sum_i act(g_i, u_i) + b2[e, h]; clamped SwiGLU with values past the limit
+    L = _small_layer(has_zeros=False, E=2)
+    E, H, I, b = 2, 64, 32, 2.0 ** -5
+    L["w13_q"] = pack_along_last(torch.full((E, 2 * I, H), 8), 4).numpy()
+    L["w2_q"] = pack_along_last(torch.full((E, H, I), 9), 4).numpy()  # (9 - 8) * s
+    L["w2_s"] = halfbits(torch.full((E, I // 32, H), b, dtype=torch.float16))
+    rng = np.random.default_rng(2)
+    L["w13_b"] = _half(rng.standard_normal((E, 2 * I)) * 8)
+    L["w2_b"] = _half(rng.standard_normal((E, H)))
+    L["topk_ids"] = np.array([[0, 1], [1, 0], [0, 1]], dtype=np.int32)
+    b13 = oracle.halfbits_to_f64(L["w13_b"], "f16")
+    b2 = oracle.halfbits_to_f64(L["w2_b"], "f16")
+    alpha, beta, lim = 1.702, 1.0, 7.0
+    y = np.zeros((E, H))
+    for e in range(E):
+        s = 0.0
+        for i in range(I):
+            g, u = b13[e, i], b13[e, I + i]
+            g, u = min(g, lim), min(max(u, -lim), lim)
+            s += g / (1.0 + math.exp(-alpha * g)) * (u + beta)
+        y[e] = b * s + b2[e]
+    tw = L["topk_w"].astype(np.float64)
+    want = np.stack([sum(tw[t, j] * y[L["topk_ids"][t, j]] for j in range(2)) for t in range(3)])
+    got = oracle.fused_moe_per_token(dict(L, glu=(alpha, beta, lim)), round_output=False)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
+    assert np.any(np.abs(b13) > lim)  # the clamp is exercised
+
+
+def test_layer_biases_grouped_matches_per_token():
+    L = _small_layer(E=4)
+    rng = np.random.default_rng(4)
+    L["w13_b"] = _half(rng.standard_normal((4, 64)))
+    L["w2_b"] = _half(rng.standard_normal((4, 64)))
+    for glu in (None, (1.702, 1.0, 0.5)):
+        a = oracle.fused_moe_per_token(dict(L, glu=glu), round_output=False)
+        b = oracle.fused_moe_grouped(dict(L, glu=glu), round_output=False)
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-15)
