@@ -288,6 +288,54 @@ wna16_status wna16_fused_moe_prepacked(const void* hidden, wna16_dtype act_dtype
                                        void* const* events);
 
 /*
+ * Model variants (vLLM fused_moe/oracle/int8.py: the int8 MoE quant config
+ * carries w1_bias / w2_bias, and passes swiglu_alpha / swiglu_beta /
+ * swiglu_limit to its clamped-SwiGLU backend; the pages give no formulas, these
+ * are the readings implemented).
+ *   w13_bias  [E, 2I] act_dtype (gate rows, then up rows) or NULL: added in
+ *             fp32 to the gate/up GEMM output before the activation.
+ *   w2_bias   [E, H] act_dtype or NULL: added in fp32 to the down GEMM output
+ *             before the top-k weight (once per (token, slot), whatever the
+ *             K split).
+ *   activation WNA16_ACT_SILU: silu(g) * u (the default layer).
+ *             WNA16_ACT_SWIGLU_CLAMP: g' * sigmoid(alpha * g') * (u' + beta)
+ *             with g' = min(g, limit), u' = clamp(u, -limit, limit) when
+ *             limit > 0 (no clamp otherwise); alpha and beta finite.
+ * A zero-initialized struct (or a NULL pointer) is the default layer. Both
+ * bias pointers must be aligned to their 2-byte elements.
+ */
+typedef enum { WNA16_ACT_SILU = 0, WNA16_ACT_SWIGLU_CLAMP = 1 } wna16_activation;
+
+typedef struct {
+  const void* w13_bias;
+  const void* w2_bias;
+  wna16_activation activation;
+  float swiglu_alpha;
+  float swiglu_beta;
+  float swiglu_limit;
+} wna16_moe_options;
+
+/*
+ * wna16_fused_moe_timed / wna16_fused_moe_prepacked with model-variant
+ * options (may be NULL). Same workspace size, errors and semantics; a bad
+ * `options` field returns WNA16_ERR_INVALID_ARG before any launch.
+ */
+wna16_status wna16_fused_moe_ex(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I,
+                                int E, int topk, const int32_t* w13_q, const void* w13_scales,
+                                const int32_t* w13_zeros, const int32_t* w2_q, const void* w2_scales,
+                                const int32_t* w2_zeros, wna16_dtype scale_dtype, int bits, int group_size,
+                                const int32_t* topk_ids, const float* topk_weights, void* out, void* workspace,
+                                size_t workspace_bytes, int block, int split_k, void* stream,
+                                void* const* events, const wna16_moe_options* options);
+wna16_status wna16_fused_moe_prepacked_ex(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
+                                          int64_t I, int E, int topk, const void* w13_packed,
+                                          const void* w2_packed, int has_zeros, wna16_dtype scale_dtype, int bits,
+                                          int group_size, const int32_t* topk_ids, const float* topk_weights,
+                                          void* out, void* workspace, size_t workspace_bytes, int block,
+                                          int split_k, void* stream, void* const* events,
+                                          const wna16_moe_options* options);
+
+/*
  * Synchronizes `stream`, then reads the device status word at the start of a
  * fused-call workspace (or any int32 status word the caller passed to the
  * align call). Writes the raw bits to *bits_out (may be NULL) and returns

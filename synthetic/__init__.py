@@ -18,6 +18,7 @@ from .workloads import (  # noqa: F401
     make_router_logits,
     routing_params,
     make_hidden,
+    make_biases,
     quantize_expert,
     pack_along_last,
 )

@@ -170,6 +170,16 @@ def make_routing(wl: Workload, M: int, seed: int):
     return ids.to(torch.int32).contiguous(), w.to(torch.float32).contiguous()
 
 
+def make_biases(wl: Workload, seed: int, device="cpu", std: float = 0.05):
+    """Per-expert biases in the activation dtype: w13 [E, 2I] (gate rows, then up
+    rows) and w2 [E, H], N(0, std^2)."""
+    g = _gen(seed, "cpu")
+    dt = _TORCH_DTYPE[wl.act_dtype]
+    b13 = (torch.randn(wl.E, 2 * wl.I, generator=g) * std).to(dt).to(device)
+    b2 = (torch.randn(wl.E, wl.H, generator=g) * std).to(dt).to(device)
+    return b13.contiguous(), b2.contiguous()
+
+
 def make_hidden(wl: Workload, M: int, seed: int, device="cpu") -> torch.Tensor:
     g = _gen(seed, device)
     x = torch.randn(M, wl.H, generator=g, device=device, dtype=torch.float32) * wl.act_std

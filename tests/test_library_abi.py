@@ -130,3 +130,30 @@ def test_routing_argument_errors_are_host_side(lib):
     assert _call_routing(lib, scoring=2) == 1
     assert _call_routing(lib, dt=3) == 1
 
+
+
+class _Opt(ctypes.Structure):
+    _fields_ = [("w13_bias", ctypes.c_void_p), ("w2_bias", ctypes.c_void_p), ("activation", ctypes.c_int),
+                ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
+                ("swiglu_limit", ctypes.c_float)]
+
+
+def _call_fused_ex(lib, opt):
+    v = ctypes.c_void_p
+    return lib.wna16_fused_moe_ex(v(16), 0, 4, 256, 512, 8, 2, v(16), v(16), None, v(16), v(16), None, 0, 4, 128,
+                                  v(16), v(16), v(16), v(16), 1 << 30, 0, 0, None, None, ctypes.byref(opt))
+
+
+def test_options_errors_are_host_side(lib):
+    nan = float("nan")
+    assert _call_fused_ex(lib, _Opt(None, None, 2, 1.0, 0.0, 0.0)) == 1  # unknown activation
+    assert _call_fused_ex(lib, _Opt(17, None, 0, 1.0, 0.0, 0.0)) == 1  # misaligned bias
+    assert _call_fused_ex(lib, _Opt(None, 33, 0, 1.0, 0.0, 0.0)) == 1
+    assert _call_fused_ex(lib, _Opt(None, None, 1, nan, 1.0, 7.0)) == 1
+    assert _call_fused_ex(lib, _Opt(None, None, 1, 1.7, float("inf"), 7.0)) == 1
+    assert _call_fused_ex(lib, _Opt(None, None, 1, 1.7, 1.0, nan)) == 1
+    v = ctypes.c_void_p
+    # M = 0 with valid options: OK, nothing launched
+    assert lib.wna16_fused_moe_ex(v(16), 0, 0, 256, 512, 8, 2, v(16), v(16), None, v(16), v(16), None, 0, 4, 128,
+                                  v(16), v(16), v(16), v(16), 1 << 30, 0, 0, None, None,
+                                  ctypes.byref(_Opt(16, 16, 1, 1.7, 1.0, 7.0))) == 0

@@ -31,12 +31,40 @@ EXPORTED = (
     "wna16_align_capacity", "wna16_moe_align_block_size", "wna16_choose_block",
     "wna16_fused_moe_workspace_bytes", "wna16_fused_moe", "wna16_fused_moe_timed",
     "wna16_fused_moe_noalloc", "wna16_prepack_bytes", "wna16_prepack", "wna16_fused_moe_prepacked",
-    "wna16_read_device_status", "wna16_status_string", "wna16_topk_routing",
+    "wna16_read_device_status", "wna16_status_string", "wna16_topk_routing", "wna16_fused_moe_ex",
+    "wna16_fused_moe_prepacked_ex",
 )
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
 _LOGIT_DTYPE = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
 _SCORING = {"softmax": 0, "sigmoid": 1}
+
+
+class MoeOptions(ctypes.Structure):
+    """``wna16_moe_options``: biases and the gate/up activation."""
+    _fields_ = [("w13_bias", ctypes.c_void_p), ("w2_bias", ctypes.c_void_p), ("activation", ctypes.c_int),
+                ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
+                ("swiglu_limit", ctypes.c_float)]
+
+
+_ACTIVATION = {"silu": 0, "swiglu_clamp": 1}
+
+
+def _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu):
+    """A MoeOptions for the given variant, or None for the default layer."""
+    if w13_bias is None and w2_bias is None and activation == "silu":
+        return None
+    if activation not in _ACTIVATION:
+        raise ValueError(f"activation must be one of {tuple(_ACTIVATION)}")
+    dev = hidden.device
+    if w13_bias is not None:
+        _check(w13_bias, "w13_bias", hidden.dtype, (E, 2 * I), dev)
+    if w2_bias is not None:
+        _check(w2_bias, "w2_bias", hidden.dtype, (E, H), dev)
+    alpha, beta, limit = swiglu
+    return MoeOptions(None if w13_bias is None else w13_bias.data_ptr(),
+                      None if w2_bias is None else w2_bias.data_ptr(), _ACTIVATION[activation],
+                      float(alpha), float(beta), float(limit))
 
 
 class WNA16Error(RuntimeError):
@@ -83,6 +111,10 @@ def load() -> ctypes.CDLL:
     L.wna16_fused_moe_prepacked.restype = i32
     L.wna16_read_device_status.argtypes = [vp, c.POINTER(c.c_int32), vp]
     L.wna16_read_device_status.restype = i32
+    L.wna16_fused_moe_ex.argtypes = L.wna16_fused_moe_timed.argtypes + [vp]
+    L.wna16_fused_moe_ex.restype = i32
+    L.wna16_fused_moe_prepacked_ex.argtypes = L.wna16_fused_moe_prepacked.argtypes + [vp]
+    L.wna16_fused_moe_prepacked_ex.restype = i32
     L.wna16_topk_routing.argtypes = [vp, i32, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     L.wna16_topk_routing.restype = i32
     L.wna16_status_string.argtypes = [i32]
@@ -194,13 +226,17 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
               w2_zeros: Optional[torch.Tensor], topk_ids: torch.Tensor, topk_weights: torch.Tensor,
               bits: int, group_size: int, out: Optional[torch.Tensor] = None,
               workspace: Optional[torch.Tensor] = None, block: int = 0, split_k: int = 0,
-              stream=None, events=None) -> torch.Tensor:
+              stream=None, events=None, w13_bias: Optional[torch.Tensor] = None,
+              w2_bias: Optional[torch.Tensor] = None, activation: str = "silu",
+              swiglu=(1.702, 1.0, 7.0)) -> torch.Tensor:
     """The fused layer (see include/wna16_moe.h). Returns ``out`` [M, H].
 
     ``events``: optional list of 6 ``torch.cuda.Event`` (or None; each must
     already exist on the device, i.e. have been recorded once) recorded before
     the align, gather, gate/up GEMM, down GEMM and combine launches and after
-    the last.
+    the last. ``w13_bias`` [E, 2I], ``w2_bias`` [E, H] (activation dtype),
+    ``activation`` "silu" or "swiglu_clamp" with ``swiglu`` = (alpha, beta,
+    limit): the model-variant options of ``wna16_fused_moe_ex``.
     """
     _check(hidden, "hidden", (torch.float16, torch.bfloat16))
     dev = hidden.device
@@ -234,7 +270,15 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
             _ptr(w13_zeros), _ptr(w2_q), _ptr(w2_scales), _ptr(w2_zeros), _DTYPE[w13_scales.dtype], bits,
             group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out), _ptr(workspace),
             workspace.numel(), block, split_k, _stream(stream))
-    if events is None:
+    opt = _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu)
+    if opt is not None:
+        arr = None
+        if events is not None:
+            if len(events) != 6:
+                raise ValueError("events must hold 6 entries")
+            arr = (ctypes.c_void_p * 6)(*[None if e is None else e.cuda_event for e in events])
+        st = load().wna16_fused_moe_ex(*args, arr, ctypes.byref(opt))
+    elif events is None:
         st = load().wna16_fused_moe(*args)
     else:
         if len(events) != 6:
@@ -309,8 +353,11 @@ def prepack(q: torch.Tensor, scales: torch.Tensor, zeros: Optional[torch.Tensor]
 def fused_moe_prepacked(hidden: torch.Tensor, w13: PackedWeights, w2: PackedWeights, topk_ids: torch.Tensor,
                         topk_weights: torch.Tensor, out: Optional[torch.Tensor] = None,
                         workspace: Optional[torch.Tensor] = None, block: int = 0, split_k: int = 0,
-                        stream=None, events=None) -> torch.Tensor:
-    """The fused layer on prepacked weights (``wna16_fused_moe_prepacked``)."""
+                        stream=None, events=None, w13_bias: Optional[torch.Tensor] = None,
+                        w2_bias: Optional[torch.Tensor] = None, activation: str = "silu",
+                        swiglu=(1.702, 1.0, 7.0)) -> torch.Tensor:
+    """The fused layer on prepacked weights (``wna16_fused_moe_prepacked``; with
+    model-variant options, ``wna16_fused_moe_prepacked_ex``)."""
     _check(hidden, "hidden", (torch.float16, torch.bfloat16))
     dev = hidden.device
     M, H = hidden.shape
@@ -337,10 +384,14 @@ def fused_moe_prepacked(hidden: torch.Tensor, w13: PackedWeights, w2: PackedWeig
         if len(events) != 6:
             raise ValueError("events must hold 6 entries")
         arr = (ctypes.c_void_p * 6)(*[None if e is None else e.cuda_event for e in events])
-    st = load().wna16_fused_moe_prepacked(
-        _ptr(hidden), _DTYPE[hidden.dtype], M, H, I, E, topk, _ptr(w13.data), _ptr(w2.data), int(w13.has_zeros),
-        _DTYPE[w13.scale_dtype], w13.bits, w13.group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out),
-        _ptr(workspace), workspace.numel(), block, split_k, _stream(stream), arr)
+    args = (_ptr(hidden), _DTYPE[hidden.dtype], M, H, I, E, topk, _ptr(w13.data), _ptr(w2.data),
+            int(w13.has_zeros), _DTYPE[w13.scale_dtype], w13.bits, w13.group_size, _ptr(topk_ids),
+            _ptr(topk_weights), _ptr(out), _ptr(workspace), workspace.numel(), block, split_k, _stream(stream), arr)
+    opt = _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu)
+    if opt is not None:
+        st = load().wna16_fused_moe_prepacked_ex(*args, ctypes.byref(opt))
+    else:
+        st = load().wna16_fused_moe_prepacked(*args)
     _raise(st, "wna16_fused_moe_prepacked")
     return out
 

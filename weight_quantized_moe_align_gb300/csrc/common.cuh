@@ -72,6 +72,9 @@ struct GemmArgs {
   float* part;                 // deferred-scale gate/up GEMM with split > 1: [tile][block][split][128][nt] fp32
   int* counters;               //   arrivals per (tile, block, lane quarter), zero between calls
   int cap;                     // rows of the expert-sorted token matrices
+  const void* bias;            // gate/up: [E, 2I], down: [E, H], activation dtype; null: none
+  int glu;                     // gate/up activation: 0 silu(g) * u, 1 clamped SwiGLU
+  float glu_alpha, glu_beta, glu_limit;
 };
 
 // One weight stage in shared memory: packed codes of 128 rows x 128 K, then up

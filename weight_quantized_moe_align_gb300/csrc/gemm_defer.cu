@@ -1,66 +1,15 @@
-// Instantiations of the deferred-scale grouped GEMM (16- and 32-token tiles).
-#include "gemm_defer.cuh"
-#include "gemm_launch.cuh"
+// Instantiations of the deferred-scale grouped GEMM, default epilogues.
+#include "gemm_defer_launch.cuh"
 
 namespace wna16 {
-
-namespace {
-
-template <int BITS, int ACT, int SCL, int GEMM, int NT>
-cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t stream, const CUtensorMap& q, const CUtensorMap& s,
-                       const CUtensorMap& z, const CUtensorMap& b, const CUtensorMap& x, const GemmArgs& a) {
-  auto* fn = moe_gemm_defer_kernel<BITS, ACT, SCL, GEMM, NT>;
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
-  fn<<<grid, kDeferThreads, smem, stream>>>(q, s, z, b, x, a);
-  return cudaGetLastError();
-}
-
-template <int BITS, int GEMM, int NT>
-cudaError_t by_dtype(int act, int scl, dim3 grid, size_t smem, cudaStream_t stream, const CUtensorMap& q,
-                     const CUtensorMap& s, const CUtensorMap& z, const CUtensorMap& b, const CUtensorMap& x,
-                     const GemmArgs& a) {
-  if constexpr (BITS == 8) {
-    if (act != 0) return cudaErrorInvalidValue;  // 8-bit codes: fp16 activations only
-    if (scl == 0) return launch_one<8, 0, 0, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
-    return launch_one<8, 0, 1, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
-  } else {
-    if (act == 0 && scl == 0) return launch_one<4, 0, 0, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
-    if (act == 0 && scl == 1) return launch_one<4, 0, 1, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
-    if (act == 1 && scl == 0) return launch_one<4, 1, 0, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
-    return launch_one<4, 1, 1, GEMM, NT>(grid, smem, stream, q, s, z, b, x, a);
-  }
-}
-
-template <int BITS, int GEMM>
-cudaError_t by_tile(int nt, int act, int scl, dim3 grid, size_t smem, cudaStream_t stream, const CUtensorMap& q,
-                    const CUtensorMap& s, const CUtensorMap& z, const CUtensorMap& b, const CUtensorMap& x,
-                    const GemmArgs& a) {
-  if (nt == 16) return by_dtype<BITS, GEMM, 16>(act, scl, grid, smem, stream, q, s, z, b, x, a);
-  if (nt == 32) return by_dtype<BITS, GEMM, 32>(act, scl, grid, smem, stream, q, s, z, b, x, a);
-  return cudaErrorInvalidValue;
-}
-
-}  // namespace
 
 bool defer_supported(int bits, int act) { return bits == 4 || (bits == 8 && act == 0); }
 
 cudaError_t launch_gemm_defer(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
                               const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                               const CUtensorMap& b, const CUtensorMap& x, const GemmArgs& a) {
-  const int nt = a.block;
-  if (bits == 4)
-    return gemm == 1 ? by_tile<4, 1>(nt, act, scl, grid, smem, stream, q, s, z, b, x, a)
-                     : by_tile<4, 2>(nt, act, scl, grid, smem, stream, q, s, z, b, x, a);
-  return gemm == 1 ? by_tile<8, 1>(nt, act, scl, grid, smem, stream, q, s, z, b, x, a)
-                   : by_tile<8, 2>(nt, act, scl, grid, smem, stream, q, s, z, b, x, a);
+  if (a.bias || a.glu) return launch_gemm_defer_var(bits, act, scl, gemm, grid, smem, stream, q, s, z, b, x, a);
+  return defer_detail::launch<0>(bits, act, scl, gemm, grid, smem, stream, q, s, z, b, x, a);
 }
 
 }  // namespace wna16

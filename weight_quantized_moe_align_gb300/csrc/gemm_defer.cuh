@@ -172,7 +172,9 @@ __device__ __forceinline__ float scale_to_f32(uint32_t bits) {
   else return __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(bits)));
 }
 
-template <int BITS, int ACT, int SCL, int GEMM, int NT>
+// VAR = 1: the model-variant epilogues (biases, clamped SwiGLU), a separate
+// instantiation so that the default one keeps its register allocation.
+template <int BITS, int ACT, int SCL, int GEMM, int NT, int VAR>
 __global__ void __launch_bounds__(kDeferThreads, 2)
     moe_gemm_defer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
                           const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_b,
@@ -525,13 +527,18 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         const bool lo = lane < 16;
         const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
         const int fp = kPermuteK<BITS> ? permute_k8(f) : f;
+        if (VAR && a.bias) {
+          const float b = bias_of<ACT>(a, unit_expert(a, w.blk), lo ? f : a.I + f);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) acc[j] += b;
+        }
 #pragma unroll
         for (int j = 0; j < NT / 2; ++j) {
           const float mine = lo ? acc[j] : acc[j + NT / 2];
           const float other = __shfl_xor_sync(0xFFFFFFFFu, lo ? acc[j + NT / 2] : acc[j], 16);
           const float gt = lo ? mine : other;
           const float up = lo ? other : mine;
-          const float val = gt / (1.0f + __expf(-gt)) * up;
+          const float val = VAR ? gate_up_act(a, gt, up) : gt / (1.0f + __expf(-gt)) * up;
           const int col = lo ? j : j + NT / 2;
           const size_t row = static_cast<size_t>(w.blk) * NT + col;
           float stored;
@@ -560,6 +567,12 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         const int hr = w.tile * kTileRows + q * 32 + lane;
         const int my_pid = a.sorted_ids[w.blk * NT + (lane & (NT - 1))];
         const float my_w = (my_pid >= 0 && my_pid < a.P) ? a.topk_w[my_pid] : 0.f;
+        if (VAR && a.bias && w.sp == 0 && hr < a.N) {
+          // the expert's bias, added once (by the first K split)
+          const float b = bias_of<ACT>(a, unit_expert(a, w.blk), hr);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) acc[j] += b;
+        }
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           const int pid = __shfl_sync(0xFFFFFFFFu, my_pid, j);

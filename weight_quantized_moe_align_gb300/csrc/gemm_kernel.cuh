@@ -44,6 +44,26 @@ struct Act<1> {
   using T2 = __nv_bfloat162;
 };
 
+// Bias of row `row` of expert e's matrix (activation dtype, as fp32).
+template <int ACT>
+__device__ __forceinline__ float bias_of(const GemmArgs& a, int e, int row) {
+  const auto* b = static_cast<const typename Act<ACT>::T*>(a.bias);
+  if constexpr (ACT == 0) return __half2float(b[static_cast<size_t>(e) * a.N + row]);
+  else return __bfloat162float(b[static_cast<size_t>(e) * a.N + row]);
+}
+
+// The gate/up activation: silu(g) * u, or (a.glu) the clamped SwiGLU
+// g' sigmoid(alpha g') (u' + beta) with g' = min(g, L), u' = clamp(u, -L, L)
+// for L = a.glu_limit > 0 (no clamp otherwise).
+__device__ __forceinline__ float gate_up_act(const GemmArgs& a, float g, float u) {
+  if (!a.glu) return g / (1.0f + __expf(-g)) * u;
+  if (a.glu_limit > 0.f) {
+    g = fminf(g, a.glu_limit);
+    u = fminf(fmaxf(u, -a.glu_limit), a.glu_limit);
+  }
+  return g / (1.0f + __expf(-a.glu_alpha * g)) * (u + a.glu_beta);
+}
+
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
@@ -198,10 +218,30 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
   if (!warp_wait_all(&accfull[acc], acc_phase, abort_flag, a.status)) return false;
   tc_fence_after();
   const uint32_t t_base = tmem + ((q * 32) << 16) + acc * NT;
+  // bias of this lane's row: gate/up GEMM, gate row f (lanes 0-15) or up row
+  // I + f (16-31); down GEMM, row h, added by the first K split only
+  float bias = 0.f;
+  bool has_bias = false;
+  if (a.bias) {
+    const int e = unit_expert(a, w.blk);
+    if (GEMM == 1) {
+      const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
+      bias = bias_of<ACT>(a, e, lane < 16 ? f : a.I + f);
+      has_bias = true;
+    } else {
+      const int h = w.tile * kTileRows + q * 32 + lane;
+      has_bias = w.sp == 0 && h < a.N;
+      if (has_bias) bias = bias_of<ACT>(a, e, h);
+    }
+  }
   for (int c0 = 0; c0 < NT; c0 += 16) {
     uint32_t v[16];
     tmem_ld16(t_base + c0, v);
     tmem_ld_wait();
+    if (has_bias) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + bias);
+    }
     if (GEMM == 1) {
       // Lanes 0-15 of this quarter hold gate rows, lanes 16-31 the up rows of
       // the same 16 features; swap halves so each lane owns 8 (feature, token)
@@ -216,14 +256,14 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
         const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, lo ? v[j + 8] : v[j], 16);
         const float g = __uint_as_float(lo ? mine : other);
         const float up = __uint_as_float(lo ? other : mine);
-        const float silu = g / (1.0f + __expf(-g));
+        const float val = gate_up_act(a, g, up);
         const int col = c0 + (lo ? j : j + 8);
         const size_t row = static_cast<size_t>(w.blk) * NT + col;
         const int fp = kPermuteK<BITS> ? permute_k8(f) : f;  // the down GEMM's K order
         if constexpr (ACT == 0)
-          act[row * a.I + fp] = __float2half_rn(silu * up);
+          act[row * a.I + fp] = __float2half_rn(val);
         else
-          act[row * a.I + fp] = __float2bfloat16_rn(silu * up);
+          act[row * a.I + fp] = __float2bfloat16_rn(val);
       }
     } else {
       float* slab = reinterpret_cast<float*>(a.out);

@@ -18,6 +18,10 @@ bool defer_supported(int bits, int act);
 cudaError_t launch_gemm_defer(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
                               const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                               const CUtensorMap& b, const CUtensorMap& x, const GemmArgs& a);
+// the same with the model-variant epilogues (a.bias or a.glu set)
+cudaError_t launch_gemm_defer_var(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
+                              const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
+                              const CUtensorMap& b, const CUtensorMap& x, const GemmArgs& a);
 
 cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* num_post_pad, int32_t* counts,

@@ -392,8 +392,16 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
                        const void* w13_pack, const void* w2_pack, int pack_zeros, wna16_dtype scale_dtype,
                        int bits, int group_size, const int32_t* topk_ids, const float* topk_weights, void* out,
                        void* workspace, size_t workspace_bytes, int block, int split_k, void* stream,
-                       void* const* events) {
+                       void* const* events, const wna16_moe_options* opt) {
   if (act_dtype != WNA16_F16 && act_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
+  if (opt) {
+    if (opt->activation != WNA16_ACT_SILU && opt->activation != WNA16_ACT_SWIGLU_CLAMP) return WNA16_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(opt->w13_bias) & 1u) || (reinterpret_cast<uintptr_t>(opt->w2_bias) & 1u))
+      return WNA16_ERR_INVALID_ARG;
+    if (opt->activation == WNA16_ACT_SWIGLU_CLAMP &&
+        (!std::isfinite(opt->swiglu_alpha) || !std::isfinite(opt->swiglu_beta) || std::isnan(opt->swiglu_limit)))
+      return WNA16_ERR_INVALID_ARG;
+  }
   if (scale_dtype != WNA16_F16 && scale_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
   Resolved r;
   const wna16_status st = resolve(M, H, I, E, topk, bits, group_size, block, split_k, &r);
@@ -519,6 +527,11 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   a1.cap = static_cast<int>(cap);
   a1.part = part1;
   a1.counters = cnt1;
+  a1.bias = opt ? opt->w13_bias : nullptr;
+  a1.glu = opt && opt->activation == WNA16_ACT_SWIGLU_CLAMP ? 1 : 0;
+  a1.glu_alpha = opt ? opt->swiglu_alpha : 1.f;
+  a1.glu_beta = opt ? opt->swiglu_beta : 0.f;
+  a1.glu_limit = opt ? opt->swiglu_limit : 0.f;
   a1.wpack = packed ? static_cast<const uint8_t*>(w13_pack) : nullptr;
   a1.wimg = prepack_image_bytes(bits, prepack_sg(r.G1), zeros ? 1 : 0);
   const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles * split1;
@@ -537,6 +550,7 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
 
   GemmArgs a2 = a1;
   a2.out = slab;
+  a2.bias = opt ? opt->w2_bias : nullptr;
   a2.K = static_cast<int>(I);
   a2.N = static_cast<int>(H);
   a2.I = 0;
@@ -582,7 +596,7 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
                                    void* stream, void* const* events) {
   return run_layer(hidden, act_dtype, M, H, I, E, topk, w13_q, w13_scales, w13_zeros, w2_q, w2_scales, w2_zeros,
                    nullptr, nullptr, 0, scale_dtype, bits, group_size, topk_ids, topk_weights, out, workspace,
-                   workspace_bytes, block, split_k, stream, events);
+                   workspace_bytes, block, split_k, stream, events, nullptr);
 }
 
 wna16_status wna16_fused_moe_prepacked(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
@@ -594,7 +608,32 @@ wna16_status wna16_fused_moe_prepacked(const void* hidden, wna16_dtype act_dtype
   if (!w13_packed || !w2_packed) return WNA16_ERR_INVALID_ARG;
   return run_layer(hidden, act_dtype, M, H, I, E, topk, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                    w13_packed, w2_packed, has_zeros, scale_dtype, bits, group_size, topk_ids, topk_weights, out,
-                   workspace, workspace_bytes, block, split_k, stream, events);
+                   workspace, workspace_bytes, block, split_k, stream, events, nullptr);
+}
+
+wna16_status wna16_fused_moe_ex(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I,
+                                int E, int topk, const int32_t* w13_q, const void* w13_scales,
+                                const int32_t* w13_zeros, const int32_t* w2_q, const void* w2_scales,
+                                const int32_t* w2_zeros, wna16_dtype scale_dtype, int bits, int group_size,
+                                const int32_t* topk_ids, const float* topk_weights, void* out, void* workspace,
+                                size_t workspace_bytes, int block, int split_k, void* stream,
+                                void* const* events, const wna16_moe_options* options) {
+  return run_layer(hidden, act_dtype, M, H, I, E, topk, w13_q, w13_scales, w13_zeros, w2_q, w2_scales, w2_zeros,
+                   nullptr, nullptr, 0, scale_dtype, bits, group_size, topk_ids, topk_weights, out, workspace,
+                   workspace_bytes, block, split_k, stream, events, options);
+}
+
+wna16_status wna16_fused_moe_prepacked_ex(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H,
+                                          int64_t I, int E, int topk, const void* w13_packed,
+                                          const void* w2_packed, int has_zeros, wna16_dtype scale_dtype, int bits,
+                                          int group_size, const int32_t* topk_ids, const float* topk_weights,
+                                          void* out, void* workspace, size_t workspace_bytes, int block,
+                                          int split_k, void* stream, void* const* events,
+                                          const wna16_moe_options* options) {
+  if (!w13_packed || !w2_packed) return WNA16_ERR_INVALID_ARG;
+  return run_layer(hidden, act_dtype, M, H, I, E, topk, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                   w13_packed, w2_packed, has_zeros, scale_dtype, bits, group_size, topk_ids, topk_weights, out,
+                   workspace, workspace_bytes, block, split_k, stream, events, options);
 }
 
 wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I,
