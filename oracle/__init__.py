@@ -11,6 +11,7 @@ from .wna16_oracle import (  # noqa: F401
     halfbits_to_f64,
     round_to_halfbits,
     dequantize_expert,
+    act_order_permutation,
     align_capacity,
     moe_align_block_size,
     routing_scores,

@@ -109,12 +109,14 @@ def unpack_zeros(zero_words: np.ndarray, bits: int) -> np.ndarray:
 
 
 def dequantize_expert(q: np.ndarray, scales_bits: np.ndarray, zero_words, bits: int,
-                      group_size: int, scale_dtype: str) -> np.ndarray:
-    """Float64 weights ``W[n, k] = (u[n, k] - z[k // G, n]) * s[k // G, n]``.
+                      group_size: int, scale_dtype: str, g_idx=None) -> np.ndarray:
+    """Float64 weights ``W[n, k] = (u[n, k] - z[g(k), n]) * s[g(k), n]``.
 
     ``q`` [N, K/pf] int32, ``scales_bits`` [K/G, N] raw half bits, ``zero_words``
     [K/G, N/pf] int32 or None (zero point ``2**(bits-1)``). ``group_size`` -1
-    means one group per output channel (G = K).
+    means one group per output channel (G = K). The group of k is ``k // G``,
+    or with act-order (GPTQ ``desc_act``; vLLM PR #14138 passes the ``g_idx``
+    tensor, empty there) ``g(k) = g_idx[k]``.
     """
     u = unpack_codes(q, bits)  # [N, K]
     N, K = u.shape
@@ -127,8 +129,20 @@ def dequantize_expert(q: np.ndarray, scales_bits: np.ndarray, zero_words, bits: 
     else:
         z = unpack_zeros(zero_words, bits).astype(np.float64)  # [K/G, N]
         assert z.shape == (K // G, N)
-    g_of_k = np.arange(K) // G
+    g_of_k = np.arange(K) // G if g_idx is None else np.asarray(g_idx, dtype=np.int64)
+    assert g_of_k.shape == (K,) and g_of_k.min() >= 0 and g_of_k.max() < K // G
     return (u.astype(np.float64) - z.T[:, g_of_k]) * s.T[:, g_of_k]
+
+
+def act_order_permutation(g_idx: np.ndarray):
+    """K order that makes act-order groups contiguous: ``perm`` lists k by
+    ascending group, ascending k within a group (a stable sort of ``g_idx``);
+    ``inv[perm[i]] = i``. Returns (perm, inv) int32."""
+    g = np.asarray(g_idx, dtype=np.int64)
+    perm = np.array(sorted(range(g.size), key=lambda k: (g[k], k)), dtype=np.int64)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size)
+    return perm.astype(np.int32), inv.astype(np.int32)
 
 
 # ----------------------------------------------------------------------------
@@ -314,12 +328,14 @@ def _bias(L, key, e, dtype):
 
 def _expert_matrices(L, e, cache):
     if e not in cache:
+        g13 = L.get("w13_g_idx")
+        g2 = L.get("w2_g_idx")
         w13 = dequantize_expert(L["w13_q"][e], L["w13_s"][e],
                                 None if L["w13_z"] is None else L["w13_z"][e],
-                                L["bits"], L["group_size"], L["scale_dtype"])
+                                L["bits"], L["group_size"], L["scale_dtype"], None if g13 is None else g13[e])
         w2 = dequantize_expert(L["w2_q"][e], L["w2_s"][e],
                                None if L["w2_z"] is None else L["w2_z"][e],
-                               L["bits"], L["group_size"], L["scale_dtype"])
+                               L["bits"], L["group_size"], L["scale_dtype"], None if g2 is None else g2[e])
         cache[e] = (w13, w2)
     return cache[e]
 
@@ -332,7 +348,9 @@ def fused_moe_per_token(L: dict, tokens=None, round_output=True):
     [E, H, I/pf], ``w2_s`` [E, I/G, H], ``w2_z`` [E, I/G, H/pf] or None,
     ``scale_dtype``, ``bits``, ``group_size``, ``topk_ids`` [M, k], ``topk_w`` [M, k]
     float32; optional ``w13_b`` [E, 2I] / ``w2_b`` [E, H] raw half bits of the
-    activation dtype (biases) and ``glu`` (see :func:`gated_activation`). For each
+    activation dtype (biases), ``glu`` (see :func:`gated_activation`) and
+    ``w13_g_idx`` [E, H] / ``w2_g_idx`` [E, I] (act-order groups, original K
+    order; see :func:`dequantize_expert`). For each
     token t and slot j with expert e = ids[t, j] in [0, E):
     g = W13[e, :I] x_t + b13[e, :I], u = W13[e, I:] x_t + b13[e, I:],
     a = act(g, u), y = W2[e] a + b2[e]; out_t = sum_j w[t, j] y_{t,j} in slot

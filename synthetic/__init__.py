@@ -20,5 +20,7 @@ from .workloads import (  # noqa: F401
     make_hidden,
     make_biases,
     quantize_expert,
+    quantize_expert_act_order,
+    make_g_idx,
     pack_along_last,
 )

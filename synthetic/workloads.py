@@ -255,6 +255,28 @@ def quantize_expert(w: torch.Tensor, bits: int, has_zeros: bool, G: int,
     return codes, s.t().contiguous(), zeros
 
 
+def make_g_idx(K: int, G: int, seed: int) -> torch.Tensor:
+    """Act-order groups (GPTQ desc_act): a seeded order of the K columns is cut
+    into groups of G, so every group holds G columns spread over K."""
+    order = torch.randperm(K, generator=_gen(seed, "cpu"))
+    g = torch.empty(K, dtype=torch.int64)
+    g[order] = torch.arange(K) // G
+    return g
+
+
+def quantize_expert_act_order(w: torch.Tensor, bits: int, has_zeros: bool, G: int, scale_dtype: str,
+                              g_idx: torch.Tensor):
+    """``quantize_expert`` with the groups of ``g_idx`` (columns k with
+    g_idx[k] = g form group g): the columns are gathered group by group,
+    quantized as contiguous groups, and the codes put back in the original
+    column order. Scales / zeros stay [K/G, N] per group."""
+    order = torch.argsort(g_idx, stable=True)
+    codes, s, z = quantize_expert(w[:, order], bits, has_zeros, G, scale_dtype)
+    back = torch.empty_like(codes)
+    back[:, order] = codes
+    return back, s, z
+
+
 # ----------------------------------------------------------------------------
 # whole layer
 # ----------------------------------------------------------------------------

@@ -476,3 +476,87 @@ def test_layer_biases_grouped_matches_per_token():
         a = oracle.fused_moe_per_token(dict(L, glu=glu), round_output=False)
         b = oracle.fused_moe_grouped(dict(L, glu=glu), round_output=False)
         np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
+# act-order (GPTQ desc_act: group of column k = g_idx[k])
+# ----------------------------------------------------------------------------
+
+def test_act_order_permutation_closed_form():
+    perm, inv = oracle.act_order_permutation(np.array([1, 0, 1, 0, 2, 2]))
+    assert perm.tolist() == [1, 3, 0, 2, 4, 5]  # group 0: k 1, 3; group 1: k 0, 2; group 2: k 4, 5
+    assert inv.tolist() == [2, 0, 3, 1, 4, 5]
+
+
+def test_act_order_default_groups_are_the_plain_layout():
+    L = _small_layer(E=2)
+    g = np.arange(64) // 32
+    a = oracle.dequantize_expert(L["w13_q"][0], L["w13_s"][0], L["w13_z"][0], 4, 32, "f16")
+    b = oracle.dequantize_expert(L["w13_q"][0], L["w13_s"][0], L["w13_z"][0], 4, 32, "f16", g_idx=g)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("bits,has_zeros,G", [(4, True, 32), (4, False, 64), (8, False, 32)])
+def test_act_order_round_trip_within_half_step(bits, has_zeros, G):
+    # the error bound holds only if every column is dequantized with its own group
+    from synthetic import make_g_idx, quantize_expert_act_order
+    K, N = 256, 48
+    w = torch.randn(N, K, generator=torch.Generator().manual_seed(bits + G)) * 0.1
+    g = make_g_idx(K, G, 11)
+    codes, s, z = quantize_expert_act_order(w, bits, has_zeros, G, "f16", g)
+    q = pack_along_last(codes, bits).numpy()
+    zw = None if z is None else pack_along_last(z, bits).numpy()
+    W = oracle.dequantize_expert(q, halfbits(s), zw, bits, G, "f16", g_idx=g.numpy())
+    step = oracle.halfbits_to_f64(halfbits(s), "f16").T[:, g.numpy()]  # [N, K] scale of each weight
+    assert np.all(np.abs(W - w.double().numpy()) <= step / 2 + 1e-12)
+    # grouping by k // G instead breaks the bound
+    W_wrong = oracle.dequantize_expert(q, halfbits(s), zw, bits, G, "f16")
+    assert not np.all(np.abs(W_wrong - w.double().numpy()) <= step / 2 + 1e-12)
+
+
+def test_act_order_repacked_columns_are_the_plain_layout():
+    # sorting the columns by group gives a plain grouped matrix:
+    # W_actorder[:, perm[i]] = W_plain(codes[:, perm])[:, i]
+    from synthetic import make_g_idx, quantize_expert_act_order
+    K, N, G = 128, 32, 32
+    w = torch.randn(N, K, generator=torch.Generator().manual_seed(5)) * 0.1
+    g = make_g_idx(K, G, 3)
+    codes, s, z = quantize_expert_act_order(w, 4, True, G, "f16", g)
+    perm, _ = oracle.act_order_permutation(g.numpy())
+    W = oracle.dequantize_expert(pack_along_last(codes, 4).numpy(), halfbits(s), pack_along_last(z, 4).numpy(), 4, G,
+                                 "f16", g_idx=g.numpy())
+    Wp = oracle.dequantize_expert(pack_along_last(codes[:, perm], 4).numpy(), halfbits(s),
+                                  pack_along_last(z, 4).numpy(), 4, G, "f16")
+    assert np.array_equal(W[:, perm], Wp)
+
+
+def test_act_order_layer_vs_scalar_brute_force():
+    from synthetic import make_g_idx
+    L = _small_layer(M=2, H=32, I=16, E=2, k=2, G=16)
+    L["w13_g_idx"] = np.stack([make_g_idx(32, 16, 20 + e).numpy() for e in range(2)])
+    L["w2_g_idx"] = np.stack([make_g_idx(16, 16, 30 + e).numpy() for e in range(2)])
+    bits, pf, mask = 4, 8, 15
+    x = oracle.halfbits_to_f64(L["x"], "f16")
+
+    def weight(name, e, n, kk):
+        word = int(L[name + "_q"][e, n, kk // pf]) & 0xFFFFFFFF
+        u = (word >> (bits * (kk % pf))) & mask
+        g = int(L[name + "_g_idx"][e, kk])
+        s = float(oracle.halfbits_to_f64(L[name + "_s"][e, g, n], "f16"))
+        zw = int(L[name + "_z"][e, g, n // pf]) & 0xFFFFFFFF
+        return (u - ((zw >> (bits * (n % pf))) & mask)) * s
+
+    out = np.zeros((2, 32))
+    for t in range(2):
+        for j in range(2):
+            e = int(L["topk_ids"][t, j])
+            a = []
+            for i in range(16):
+                gs = sum(weight("w13", e, i, kk) * x[t, kk] for kk in range(32))
+                us = sum(weight("w13", e, 16 + i, kk) * x[t, kk] for kk in range(32))
+                a.append(gs / (1.0 + math.exp(-gs)) * us)
+            for h in range(32):
+                out[t, h] += float(L["topk_w"][t, j]) * sum(weight("w2", e, h, i) * a[i] for i in range(16))
+    got = oracle.fused_moe_per_token(L, round_output=False)
+    np.testing.assert_allclose(got, out, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(oracle.fused_moe_grouped(L, round_output=False), out, rtol=1e-12, atol=1e-15)
