@@ -66,7 +66,8 @@ typedef enum {
   WNA16_ERR_WORKSPACE_TOO_SMALL = 3,
   WNA16_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
   WNA16_ERR_DEVICE_BAD_EXPERT_ID = 5, /* device: an id outside [0, E) was dropped */
-  WNA16_ERR_DEVICE_TIMEOUT = 6        /* device: a pipeline wait gave up */
+  WNA16_ERR_DEVICE_TIMEOUT = 6,       /* device: a pipeline wait gave up */
+  WNA16_ERR_DEVICE_BAD_GROUPS = 7     /* device: act-order g_idx is not a split into groups of G */
 } wna16_status;
 
 /* Element types. Activations, outputs and scales: F16 or BF16; F32 only for
@@ -79,6 +80,7 @@ typedef enum { WNA16_SCORE_SOFTMAX = 0, WNA16_SCORE_SIGMOID = 1 } wna16_scoring;
 /* Device status bits (the int32 at offset 0 of the fused-call workspace). */
 #define WNA16_DEV_BAD_EXPERT_ID 0x1
 #define WNA16_DEV_TIMEOUT 0x2
+#define WNA16_DEV_BAD_GROUPS 0x4
 
 /*
  * Capacity of the align outputs: an upper bound on padded slots for
@@ -301,8 +303,19 @@ wna16_status wna16_fused_moe_prepacked(const void* hidden, wna16_dtype act_dtype
  *             WNA16_ACT_SWIGLU_CLAMP: g' * sigmoid(alpha * g') * (u' + beta)
  *             with g' = min(g, limit), u' = clamp(u, -limit, limit) when
  *             limit > 0 (no clamp otherwise); alpha and beta finite.
+ *   w13_perm  [E, H] int32 or NULL: act-order gate/up weights, repacked by
+ *             wna16_act_order_prepare; entry i is the original hidden index
+ *             of repacked column i (its `perm`). The layer reads each routed
+ *             token row in this order.
+ *   w2_inv_perm [E, I] int32 or NULL: act-order down weights, repacked;
+ *             entry f is the repacked column of intermediate feature f (the
+ *             prepare call's `inv_perm`).
+ *             With either permutation the layer runs the general GEMM kernel
+ *             (the 16-token deferred-scale kernel needs contiguous feature
+ *             runs). Out-of-range entries are skipped, never dereferenced.
  * A zero-initialized struct (or a NULL pointer) is the default layer. Both
- * bias pointers must be aligned to their 2-byte elements.
+ * bias pointers must be aligned to their 2-byte elements, the permutations to
+ * 4 bytes.
  */
 typedef enum { WNA16_ACT_SILU = 0, WNA16_ACT_SWIGLU_CLAMP = 1 } wna16_activation;
 
@@ -313,7 +326,34 @@ typedef struct {
   float swiglu_alpha;
   float swiglu_beta;
   float swiglu_limit;
+  const int32_t* w13_perm;
+  const int32_t* w2_inv_perm;
 } wna16_moe_options;
+
+/*
+ * Act-order (GPTQ desc_act) weights: column k of expert e belongs to group
+ * g_idx[e, k] (vLLM PR #14138 passes `g_idx` and `sort_indices` to the marlin
+ * GEMM; empty in its benchmark). This call lists each expert's columns by
+ * ascending group, ascending k within a group:
+ *   perm     [E, K] int32 out: perm[e, i] = original column of column i;
+ *   inv_perm [E, K] int32 out or NULL: inv_perm[e, perm[e, i]] = i;
+ *   q_out    [E, N, K/pf] int32 out or NULL (then q must be NULL too): the codes
+ *            of q [E, N, K/pf] (layout as in the header) with column i taken
+ *            from column perm[e, i]. With group_size G, repacked column i is in
+ *            group i / G, so q_out with the unchanged scales and zero points
+ *            [E, K/G, ...] is a plain grouped matrix for the layer calls (and
+ *            for wna16_prepack).
+ *   g_idx    [E, K] int32. Every group must hold exactly G columns (as GPTQ
+ *            writes them); otherwise WNA16_DEV_BAD_GROUPS is or-ed into
+ *            *device_status (not reset by this call) and the outputs, though
+ *            in range, are meaningless.
+ * Pass perm as the gate/up GEMM's w13_perm (K = H) and inv_perm of the down
+ * weights as w2_inv_perm (K = I) in wna16_moe_options. One-off conversion
+ * (a CTA per expert scans its g_idx once per group): not a per-call step.
+ */
+wna16_status wna16_act_order_prepare(const int32_t* q, const int32_t* g_idx, int E, int64_t N, int64_t K,
+                                     int bits, int group_size, int32_t* q_out, int32_t* perm, int32_t* inv_perm,
+                                     int32_t* device_status, void* stream);
 
 /*
  * wna16_fused_moe_timed / wna16_fused_moe_prepacked with model-variant
@@ -338,9 +378,10 @@ wna16_status wna16_fused_moe_prepacked_ex(const void* hidden, wna16_dtype act_dt
 /*
  * Synchronizes `stream`, then reads the device status word at the start of a
  * fused-call workspace (or any int32 status word the caller passed to the
- * align call). Writes the raw bits to *bits_out (may be NULL) and returns
- * WNA16_OK, WNA16_ERR_DEVICE_TIMEOUT or WNA16_ERR_DEVICE_BAD_EXPERT_ID
- * (timeout wins), or WNA16_ERR_CUDA if the copy fails. For tests and debugging.
+ * align call, or wna16_act_order_prepare). Writes the raw bits to *bits_out
+ * (may be NULL) and returns WNA16_OK, WNA16_ERR_DEVICE_TIMEOUT,
+ * WNA16_ERR_DEVICE_BAD_EXPERT_ID or WNA16_ERR_DEVICE_BAD_GROUPS (in that order
+ * of precedence), or WNA16_ERR_CUDA if the copy fails. For tests and debugging.
  */
 wna16_status wna16_read_device_status(const void* status_word, int32_t* bits_out, void* stream);
 

@@ -56,7 +56,7 @@ def test_block_choice(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         assert lib.wna16_status_string(code)
 
 
@@ -135,7 +135,7 @@ def test_routing_argument_errors_are_host_side(lib):
 class _Opt(ctypes.Structure):
     _fields_ = [("w13_bias", ctypes.c_void_p), ("w2_bias", ctypes.c_void_p), ("activation", ctypes.c_int),
                 ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
-                ("swiglu_limit", ctypes.c_float)]
+                ("swiglu_limit", ctypes.c_float), ("w13_perm", ctypes.c_void_p), ("w2_inv_perm", ctypes.c_void_p)]
 
 
 def _call_fused_ex(lib, opt):
@@ -152,8 +152,25 @@ def test_options_errors_are_host_side(lib):
     assert _call_fused_ex(lib, _Opt(None, None, 1, nan, 1.0, 7.0)) == 1
     assert _call_fused_ex(lib, _Opt(None, None, 1, 1.7, float("inf"), 7.0)) == 1
     assert _call_fused_ex(lib, _Opt(None, None, 1, 1.7, 1.0, nan)) == 1
+    assert _call_fused_ex(lib, _Opt(None, None, 0, 1.0, 0.0, 0.0, 18, None)) == 1  # misaligned permutation
+    assert _call_fused_ex(lib, _Opt(None, None, 0, 1.0, 0.0, 0.0, None, 34)) == 1
     v = ctypes.c_void_p
     # M = 0 with valid options: OK, nothing launched
     assert lib.wna16_fused_moe_ex(v(16), 0, 0, 256, 512, 8, 2, v(16), v(16), None, v(16), v(16), None, 0, 4, 128,
                                   v(16), v(16), v(16), v(16), 1 << 30, 0, 0, None, None,
                                   ctypes.byref(_Opt(16, 16, 1, 1.7, 1.0, 7.0))) == 0
+
+
+def test_act_order_prepare_errors_are_host_side(lib):
+    v = ctypes.c_void_p
+    defaults = (("q", v(16)), ("g", v(16)), ("E", 4), ("N", 256), ("K", 512), ("bits", 4), ("G", 128),
+                ("qo", v(16)), ("perm", v(16)), ("inv", None), ("st", v(16)))
+    call = lambda **o: lib.wna16_act_order_prepare(*[o.get(k, d) for k, d in defaults], None)
+    assert call(G=0) == 1
+    assert call(G=-1) == 1  # one group per channel has no order to restore
+    assert call(G=96) == 2  # K % G != 0
+    assert call(bits=3) == 1
+    assert call(q=None) == 1  # q and q_out go together
+    assert call(q=None, qo=None, perm=None) == 1
+    assert call(st=None) == 1
+    assert call(perm=v(18)) == 1

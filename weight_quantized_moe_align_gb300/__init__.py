@@ -3,9 +3,11 @@ GB300 GPU: a C-ABI CUDA library (``include/wna16_moe.h``) and its binding.
 """
 from .binding import (  # noqa: F401
     DEV_BAD_EXPERT_ID,
+    DEV_BAD_GROUPS,
     DEV_TIMEOUT,
     EXPORTED,
     PackedWeights,
+    act_order_prepare,
     WNA16Error,
     align_capacity,
     choose_block,

@@ -21,10 +21,11 @@ WNA16_OK = 0
 STATUS_NAMES = {
     0: "WNA16_OK", 1: "WNA16_ERR_INVALID_ARG", 2: "WNA16_ERR_UNSUPPORTED",
     3: "WNA16_ERR_WORKSPACE_TOO_SMALL", 4: "WNA16_ERR_CUDA",
-    5: "WNA16_ERR_DEVICE_BAD_EXPERT_ID", 6: "WNA16_ERR_DEVICE_TIMEOUT",
+    5: "WNA16_ERR_DEVICE_BAD_EXPERT_ID", 6: "WNA16_ERR_DEVICE_TIMEOUT", 7: "WNA16_ERR_DEVICE_BAD_GROUPS",
 }
 DEV_BAD_EXPERT_ID = 0x1
 DEV_TIMEOUT = 0x2
+DEV_BAD_GROUPS = 0x4
 
 # Every symbol include/wna16_moe.h declares.
 EXPORTED = (
@@ -32,7 +33,7 @@ EXPORTED = (
     "wna16_fused_moe_workspace_bytes", "wna16_fused_moe", "wna16_fused_moe_timed",
     "wna16_fused_moe_noalloc", "wna16_prepack_bytes", "wna16_prepack", "wna16_fused_moe_prepacked",
     "wna16_read_device_status", "wna16_status_string", "wna16_topk_routing", "wna16_fused_moe_ex",
-    "wna16_fused_moe_prepacked_ex",
+    "wna16_fused_moe_prepacked_ex", "wna16_act_order_prepare",
 )
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
@@ -44,15 +45,15 @@ class MoeOptions(ctypes.Structure):
     """``wna16_moe_options``: biases and the gate/up activation."""
     _fields_ = [("w13_bias", ctypes.c_void_p), ("w2_bias", ctypes.c_void_p), ("activation", ctypes.c_int),
                 ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
-                ("swiglu_limit", ctypes.c_float)]
+                ("swiglu_limit", ctypes.c_float), ("w13_perm", ctypes.c_void_p), ("w2_inv_perm", ctypes.c_void_p)]
 
 
 _ACTIVATION = {"silu": 0, "swiglu_clamp": 1}
 
 
-def _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu):
+def _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu, w13_perm=None, w2_inv_perm=None):
     """A MoeOptions for the given variant, or None for the default layer."""
-    if w13_bias is None and w2_bias is None and activation == "silu":
+    if w13_bias is None and w2_bias is None and activation == "silu" and w13_perm is None and w2_inv_perm is None:
         return None
     if activation not in _ACTIVATION:
         raise ValueError(f"activation must be one of {tuple(_ACTIVATION)}")
@@ -61,10 +62,16 @@ def _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu):
         _check(w13_bias, "w13_bias", hidden.dtype, (E, 2 * I), dev)
     if w2_bias is not None:
         _check(w2_bias, "w2_bias", hidden.dtype, (E, H), dev)
+    if w13_perm is not None:
+        _check(w13_perm, "w13_perm", torch.int32, (E, H), dev)
+    if w2_inv_perm is not None:
+        _check(w2_inv_perm, "w2_inv_perm", torch.int32, (E, I), dev)
     alpha, beta, limit = swiglu
     return MoeOptions(None if w13_bias is None else w13_bias.data_ptr(),
                       None if w2_bias is None else w2_bias.data_ptr(), _ACTIVATION[activation],
-                      float(alpha), float(beta), float(limit))
+                      float(alpha), float(beta), float(limit),
+                      None if w13_perm is None else w13_perm.data_ptr(),
+                      None if w2_inv_perm is None else w2_inv_perm.data_ptr())
 
 
 class WNA16Error(RuntimeError):
@@ -115,6 +122,8 @@ def load() -> ctypes.CDLL:
     L.wna16_fused_moe_ex.restype = i32
     L.wna16_fused_moe_prepacked_ex.argtypes = L.wna16_fused_moe_prepacked.argtypes + [vp]
     L.wna16_fused_moe_prepacked_ex.restype = i32
+    L.wna16_act_order_prepare.argtypes = [vp, vp, i32, i64, i64, i32, i32, vp, vp, vp, vp, vp]
+    L.wna16_act_order_prepare.restype = i32
     L.wna16_topk_routing.argtypes = [vp, i32, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     L.wna16_topk_routing.restype = i32
     L.wna16_status_string.argtypes = [i32]
@@ -228,7 +237,8 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
               workspace: Optional[torch.Tensor] = None, block: int = 0, split_k: int = 0,
               stream=None, events=None, w13_bias: Optional[torch.Tensor] = None,
               w2_bias: Optional[torch.Tensor] = None, activation: str = "silu",
-              swiglu=(1.702, 1.0, 7.0)) -> torch.Tensor:
+              swiglu=(1.702, 1.0, 7.0), w13_perm: Optional[torch.Tensor] = None,
+              w2_inv_perm: Optional[torch.Tensor] = None) -> torch.Tensor:
     """The fused layer (see include/wna16_moe.h). Returns ``out`` [M, H].
 
     ``events``: optional list of 6 ``torch.cuda.Event`` (or None; each must
@@ -236,7 +246,9 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
     the align, gather, gate/up GEMM, down GEMM and combine launches and after
     the last. ``w13_bias`` [E, 2I], ``w2_bias`` [E, H] (activation dtype),
     ``activation`` "silu" or "swiglu_clamp" with ``swiglu`` = (alpha, beta,
-    limit): the model-variant options of ``wna16_fused_moe_ex``.
+    limit), and for act-order weights repacked by :func:`act_order_prepare`
+    ``w13_perm`` [E, H] / ``w2_inv_perm`` [E, I]: the model-variant options of
+    ``wna16_fused_moe_ex``.
     """
     _check(hidden, "hidden", (torch.float16, torch.bfloat16))
     dev = hidden.device
@@ -270,7 +282,7 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
             _ptr(w13_zeros), _ptr(w2_q), _ptr(w2_scales), _ptr(w2_zeros), _DTYPE[w13_scales.dtype], bits,
             group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out), _ptr(workspace),
             workspace.numel(), block, split_k, _stream(stream))
-    opt = _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu)
+    opt = _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu, w13_perm, w2_inv_perm)
     if opt is not None:
         arr = None
         if events is not None:
@@ -355,7 +367,8 @@ def fused_moe_prepacked(hidden: torch.Tensor, w13: PackedWeights, w2: PackedWeig
                         workspace: Optional[torch.Tensor] = None, block: int = 0, split_k: int = 0,
                         stream=None, events=None, w13_bias: Optional[torch.Tensor] = None,
                         w2_bias: Optional[torch.Tensor] = None, activation: str = "silu",
-                        swiglu=(1.702, 1.0, 7.0)) -> torch.Tensor:
+                        swiglu=(1.702, 1.0, 7.0), w13_perm: Optional[torch.Tensor] = None,
+                        w2_inv_perm: Optional[torch.Tensor] = None) -> torch.Tensor:
     """The fused layer on prepacked weights (``wna16_fused_moe_prepacked``; with
     model-variant options, ``wna16_fused_moe_prepacked_ex``)."""
     _check(hidden, "hidden", (torch.float16, torch.bfloat16))
@@ -387,7 +400,7 @@ def fused_moe_prepacked(hidden: torch.Tensor, w13: PackedWeights, w2: PackedWeig
     args = (_ptr(hidden), _DTYPE[hidden.dtype], M, H, I, E, topk, _ptr(w13.data), _ptr(w2.data),
             int(w13.has_zeros), _DTYPE[w13.scale_dtype], w13.bits, w13.group_size, _ptr(topk_ids),
             _ptr(topk_weights), _ptr(out), _ptr(workspace), workspace.numel(), block, split_k, _stream(stream), arr)
-    opt = _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu)
+    opt = _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu, w13_perm, w2_inv_perm)
     if opt is not None:
         st = load().wna16_fused_moe_prepacked_ex(*args, ctypes.byref(opt))
     else:
@@ -396,10 +409,33 @@ def fused_moe_prepacked(hidden: torch.Tensor, w13: PackedWeights, w2: PackedWeig
     return out
 
 
+def act_order_prepare(q: torch.Tensor, g_idx: torch.Tensor, bits: int, group_size: int,
+                      status: Optional[torch.Tensor] = None, stream=None):
+    """Act-order weights -> (q_out, perm, inv_perm) by ``wna16_act_order_prepare``:
+    codes [E, N, K/pf] with the columns sorted by group, and the permutations
+    [E, K]. ``status`` (int32 [1], zeroed here if not given) receives
+    DEV_BAD_GROUPS if ``g_idx`` [E, K] is not a split into groups of G."""
+    _check(q, "q", torch.int32)
+    dev = q.device
+    E, N, kw = q.shape
+    K = kw * (32 // bits)
+    _check(g_idx, "g_idx", torch.int32, (E, K), dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(status, "status", torch.int32, (1,), dev)
+    q_out = torch.empty_like(q)
+    perm = torch.empty(E, K, dtype=torch.int32, device=dev)
+    inv = torch.empty(E, K, dtype=torch.int32, device=dev)
+    st = load().wna16_act_order_prepare(_ptr(q), _ptr(g_idx), E, N, K, bits, group_size, _ptr(q_out), _ptr(perm),
+                                        _ptr(inv), _ptr(status), _stream(stream))
+    _raise(st, "wna16_act_order_prepare")
+    return q_out, perm, inv
+
+
 def read_device_status(status_word: torch.Tensor, stream=None) -> int:
     """Synchronizes the stream and returns the raw device status bits."""
     bits = ctypes.c_int32(0)
     st = load().wna16_read_device_status(_ptr(status_word), ctypes.byref(bits), _stream(stream))
-    if st not in (0, 5, 6):
+    if st not in (0, 5, 6, 7):
         _raise(st, "wna16_read_device_status")
     return int(bits.value)

@@ -221,6 +221,40 @@ __global__ void __launch_bounds__(256)
   for (long long i = first; i < zero_n2; i += stride) zero2[i] = 0.f;
 }
 
+// Act-order gate/up weights: routed row p's expert e reads its hidden row in
+// that expert's K order, x_sorted[slot][i] = hidden[t][kperm[e][i]]. One thread
+// per 8 consecutive outputs; the int4 pair order of the GEMM (`permute`) is
+// applied to the permuted values.
+__global__ void __launch_bounds__(256)
+    moe_gather_perm_kernel(const uint16_t* __restrict__ hidden, const int32_t* __restrict__ ids,
+                           const int32_t* __restrict__ slot_of_pair, const int32_t* __restrict__ kperm, int P,
+                           int topk, int E, int H, int permute, uint4* __restrict__ x_sorted) {
+  const int h8 = H / 8;
+  const long long n = static_cast<long long>(P) * h8;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n; idx += stride) {
+    const int p = static_cast<int>(idx / h8);
+    const int c = static_cast<int>(idx % h8);
+    const int e = ids[p];
+    if (e < 0 || e >= E) continue;
+    const uint16_t* src = hidden + static_cast<long long>(p / topk) * H;
+    const int32_t* kp = kperm + static_cast<long long>(e) * H + c * 8;
+    uint32_t v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int k = kp[j];
+      v[j] = static_cast<unsigned>(k) < static_cast<unsigned>(H) ? src[k] : 0u;  // caller's table: never trusted
+    }
+    uint4 o;
+    if (permute) {  // (x0 x4)(x1 x5)(x2 x6)(x3 x7)
+      o = make_uint4(v[0] | (v[4] << 16), v[1] | (v[5] << 16), v[2] | (v[6] << 16), v[3] | (v[7] << 16));
+    } else {
+      o = make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
+    }
+    x_sorted[static_cast<long long>(slot_of_pair[p]) * h8 + c] = o;
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ T from_f32(float v);
 template <>
@@ -286,6 +320,20 @@ cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t*
                                                          topk, E, h8, permute, static_cast<uint4*>(x_sorted), xs,
                                                          cap, zero_ptr0, zero_n0, zero_ptr1, zero_n1, zero_ptr2,
                                                          zero_n2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_perm(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair,
+                               const int32_t* kperm, int P, int topk, int E, int H, int permute, int max_ctas,
+                               void* x_sorted, cudaStream_t stream) {
+  const long long n = static_cast<long long>(P) * (H / 8);
+  const int threads = 256;
+  const long long want = (n + threads - 1) / threads;
+  const unsigned blocks = static_cast<unsigned>(want < max_ctas ? want : max_ctas);
+  if (blocks == 0) return cudaSuccess;
+  moe_gather_perm_kernel<<<blocks, threads, 0, stream>>>(static_cast<const uint16_t*>(hidden), ids, slot_of_pair,
+                                                         kperm, P, topk, E, H, permute,
+                                                         static_cast<uint4*>(x_sorted));
   return cudaGetLastError();
 }
 

@@ -75,6 +75,7 @@ struct GemmArgs {
   const void* bias;            // gate/up: [E, 2I], down: [E, H], activation dtype; null: none
   int glu;                     // gate/up activation: 0 silu(g) * u, 1 clamped SwiGLU
   float glu_alpha, glu_beta, glu_limit;
+  const int32_t* act_pos;      // gate/up GEMM, act-order down weights: [E, I] column of feature f in the act cache
 };
 
 // One weight stage in shared memory: packed codes of 128 rows x 128 K, then up

@@ -222,6 +222,19 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
   // I + f (16-31); down GEMM, row h, added by the first K split only
   float bias = 0.f;
   bool has_bias = false;
+  // gate/up GEMM: the act-cache column of this lane's feature in the down
+  // GEMM's K order (act-order position, then the int4 pair order)
+  int fp = 0;
+  bool fp_ok = true;
+  if (GEMM == 1) {
+    const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
+    int pos = f;
+    if (a.act_pos) {
+      pos = a.act_pos[static_cast<size_t>(unit_expert(a, w.blk)) * a.I + f];
+      fp_ok = static_cast<unsigned>(pos) < static_cast<unsigned>(a.I);
+    }
+    fp = kPermuteK<BITS> ? permute_k8(pos) : pos;
+  }
   if (a.bias) {
     const int e = unit_expert(a, w.blk);
     if (GEMM == 1) {
@@ -249,7 +262,6 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
       using T = typename Act<ACT>::T;
       T* act = reinterpret_cast<T*>(a.out);
       const bool lo = lane < 16;
-      const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint32_t mine = lo ? v[j] : v[j + 8];
@@ -259,7 +271,7 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
         const float val = gate_up_act(a, g, up);
         const int col = c0 + (lo ? j : j + 8);
         const size_t row = static_cast<size_t>(w.blk) * NT + col;
-        const int fp = kPermuteK<BITS> ? permute_k8(f) : f;  // the down GEMM's K order
+        if (!fp_ok) continue;
         if constexpr (ACT == 0)
           act[row * a.I + fp] = __float2half_rn(val);
         else

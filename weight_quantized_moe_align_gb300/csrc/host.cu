@@ -398,6 +398,8 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
     if (opt->activation != WNA16_ACT_SILU && opt->activation != WNA16_ACT_SWIGLU_CLAMP) return WNA16_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(opt->w13_bias) & 1u) || (reinterpret_cast<uintptr_t>(opt->w2_bias) & 1u))
       return WNA16_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(opt->w13_perm) & 3u) || (reinterpret_cast<uintptr_t>(opt->w2_inv_perm) & 3u))
+      return WNA16_ERR_INVALID_ARG;
     if (opt->activation == WNA16_ACT_SWIGLU_CLAMP &&
         (!std::isfinite(opt->swiglu_alpha) || !std::isfinite(opt->swiglu_beta) || std::isnan(opt->swiglu_limit)))
       return WNA16_ERR_INVALID_ARG;
@@ -443,7 +445,11 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   // 16- and 32-token tiles run the deferred-scale kernel when every stage lies
   // in one group (G >= 128) and the code/activation formats have a
   // magic-number form.
-  const bool defer = defer_tile(B) && r.G1 >= kTileK && r.G2 >= kTileK && defer_supported(bits, act_dtype);
+  // Act-order weights run the general kernel: the deferred-scale kernel's
+  // token sums assume contiguous feature runs.
+  const bool act_order = opt && (opt->w13_perm || opt->w2_inv_perm);
+  const bool defer =
+      !act_order && defer_tile(B) && r.G1 >= kTileK && r.G2 >= kTileK && defer_supported(bits, act_dtype);
   const int kt1 = static_cast<int>((H + kTileK - 1) / kTileK);
   const int kt2 = static_cast<int>((I + kTileK - 1) / kTileK);
   float* xs1 = defer ? reinterpret_cast<float*>(ws + L.xs1) : nullptr;
@@ -489,7 +495,12 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   float* part1 = split1 > 1 ? reinterpret_cast<float*>(ws + L.part1) : nullptr;
   int* cnt1 = split1 > 1 ? reinterpret_cast<int*>(ws + L.cnt1) : nullptr;
   const int cnt1_n = split1 > 1 ? static_cast<int>((I / kGateUpRows) * max_blocks * 4) : 0;
-  if (!mark(1) || launch_gather(hidden, topk_ids, slot_of_pair, P, topk, E, static_cast<int>(H), bits == 4 ? 1 : 0,
+  if (opt && opt->w13_perm) {
+    if (!mark(1) || launch_gather_perm(hidden, topk_ids, slot_of_pair, opt->w13_perm, P, topk, E,
+                                       static_cast<int>(H), bits == 4 ? 1 : 0, sm_count() * 8, x_sorted,
+                                       s) != cudaSuccess)
+      return WNA16_ERR_CUDA;
+  } else if (!mark(1) || launch_gather(hidden, topk_ids, slot_of_pair, P, topk, E, static_cast<int>(H), bits == 4 ? 1 : 0,
                                 act_dtype, sm_count() * 8, x_sorted, xs1, static_cast<int>(cap), zero1, zero1_n,
                                 zero2, zero2_n, reinterpret_cast<float*>(cnt1), cnt1_n, s) != cudaSuccess)
     return WNA16_ERR_CUDA;
@@ -532,6 +543,7 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   a1.glu_alpha = opt ? opt->swiglu_alpha : 1.f;
   a1.glu_beta = opt ? opt->swiglu_beta : 0.f;
   a1.glu_limit = opt ? opt->swiglu_limit : 0.f;
+  a1.act_pos = opt ? opt->w2_inv_perm : nullptr;
   a1.wpack = packed ? static_cast<const uint8_t*>(w13_pack) : nullptr;
   a1.wimg = prepack_image_bytes(bits, prepack_sg(r.G1), zeros ? 1 : 0);
   const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles * split1;
@@ -657,6 +669,7 @@ wna16_status wna16_read_device_status(const void* status_word, int32_t* bits_out
   if (bits_out) *bits_out = v;
   if (v & WNA16_DEV_TIMEOUT) return WNA16_ERR_DEVICE_TIMEOUT;
   if (v & WNA16_DEV_BAD_EXPERT_ID) return WNA16_ERR_DEVICE_BAD_EXPERT_ID;
+  if (v & WNA16_DEV_BAD_GROUPS) return WNA16_ERR_DEVICE_BAD_GROUPS;
   return WNA16_OK;
 }
 
@@ -669,6 +682,7 @@ const char* wna16_status_string(wna16_status status) {
     case WNA16_ERR_CUDA: return "CUDA call failed";
     case WNA16_ERR_DEVICE_BAD_EXPERT_ID: return "device: expert id out of range (pair dropped)";
     case WNA16_ERR_DEVICE_TIMEOUT: return "device: pipeline wait timed out";
+    case WNA16_ERR_DEVICE_BAD_GROUPS: return "device: act-order g_idx is not a split into groups of G";
   }
   return "unknown status";
 }
