@@ -12,6 +12,10 @@ from .wna16_oracle import (  # noqa: F401
     round_to_halfbits,
     dequantize_expert,
     act_order_permutation,
+    AWQ_PACK_ORDER,
+    unpack_gptq_qweight,
+    unpack_gptq_qzeros,
+    unpack_awq,
     align_capacity,
     moe_align_block_size,
     routing_scores,

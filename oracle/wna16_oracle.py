@@ -146,6 +146,53 @@ def act_order_permutation(g_idx: np.ndarray):
 
 
 # ----------------------------------------------------------------------------
+# checkpoint formats (vLLM PR #12185: the fused kernel's weight format "is
+# just compatible with gptq/awq"; the formats themselves are those of the
+# public GPTQ and AWQ packers, restated here)
+# ----------------------------------------------------------------------------
+#
+# GPTQ: qweight [K/pf, N] int32, the codes of column n packed along K (word r
+#   holds k = r*pf + j in bits [bits*j, +bits)); qzeros [K/G, N/pf] packed along
+#   N the same way, storing z - 1 in the original format ("v1") and z itself in
+#   the later one ("v2"); scales [K/G, N].
+# AWQ (4-bit): qweight [K, N/8] int32 packed along N with the field order
+#   AWQ_PACK_ORDER (field i of word c holds column 8c + AWQ_PACK_ORDER[i]);
+#   qzeros [K/G, N/8] packed the same way; scales [K/G, N]; zero points stored
+#   as they are.
+
+AWQ_PACK_ORDER = (0, 2, 4, 6, 1, 3, 5, 7)
+
+
+def _fields(words: np.ndarray, bits: int) -> np.ndarray:
+    """[..., W] int32 words -> [..., W, 32/bits] fields, LSB first."""
+    w = np.asarray(words).astype(np.int64) & 0xFFFFFFFF
+    pf = 32 // bits
+    shifts = bits * np.arange(pf)
+    return (w[..., None] >> shifts) & ((1 << bits) - 1)
+
+
+def unpack_gptq_qweight(qweight: np.ndarray, bits: int) -> np.ndarray:
+    """GPTQ qweight [K/pf, N] -> codes [N, K]."""
+    f = _fields(qweight, bits)  # [K/pf, N, pf]: field j of word (r, n) is k = r*pf + j
+    Kw, N, pf = f.shape
+    return np.transpose(f, (1, 0, 2)).reshape(N, Kw * pf)
+
+
+def unpack_gptq_qzeros(qzeros: np.ndarray, bits: int, stored_minus_one: bool = True) -> np.ndarray:
+    """GPTQ qzeros [K/G, N/pf] -> zero points [K/G, N] (v1 adds the 1 back, mod 2^bits)."""
+    z = _fields(qzeros, bits).reshape(qzeros.shape[0], -1)
+    return (z + 1) % (1 << bits) if stored_minus_one else z
+
+
+def unpack_awq(words: np.ndarray) -> np.ndarray:
+    """AWQ words [R, N/8] (4-bit, interleaved) -> values [R, N] in column order."""
+    f = _fields(words, 4)  # [R, N/8, 8]: field i holds column 8c + AWQ_PACK_ORDER[i]
+    out = np.empty_like(f)
+    out[..., list(AWQ_PACK_ORDER)] = f
+    return out.reshape(f.shape[0], -1)
+
+
+# ----------------------------------------------------------------------------
 # moe_align_block_size
 # ----------------------------------------------------------------------------
 

@@ -560,3 +560,77 @@ def test_act_order_layer_vs_scalar_brute_force():
     got = oracle.fused_moe_per_token(L, round_output=False)
     np.testing.assert_allclose(got, out, rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(oracle.fused_moe_grouped(L, round_output=False), out, rtol=1e-12, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
+# GPTQ / AWQ checkpoint formats
+# ----------------------------------------------------------------------------
+
+def test_awq_field_order_literal_word():
+    # field i holds column AWQ_PACK_ORDER[i]: 0x76543210 puts 0..7 in columns 0 2 4 6 1 3 5 7
+    assert oracle.unpack_awq(np.array([[0x76543210]])).tolist() == [[0, 4, 1, 5, 2, 6, 3, 7]]
+    assert oracle.unpack_awq(np.array([[0x0000000F, 0xF0000000]])).tolist() == [[15] + [0] * 7 + [0] * 7 + [15]]
+
+
+def test_gptq_literal_words():
+    # column n of word row r holds k = 8 r + j in field j
+    q = np.array([[0x76543210, 0x00000010], [0x00000000, 0xF0000000]])
+    codes = oracle.unpack_gptq_qweight(q, 4)
+    assert codes.shape == (2, 16)
+    assert codes[0].tolist() == list(range(8)) + [0] * 8
+    assert codes[1].tolist() == [0, 1] + [0] * 13 + [15]
+    q8 = np.array([[0x04030201]])
+    assert oracle.unpack_gptq_qweight(q8, 8).tolist() == [[1, 2, 3, 4]]
+    # v1 zero points: stored z - 1, so 0xF is zero point 0
+    assert oracle.unpack_gptq_qzeros(np.array([[0x7654321F]]), 4).tolist() == [[0, 2, 3, 4, 5, 6, 7, 8]]
+    assert oracle.unpack_gptq_qzeros(np.array([[0x7654321F]]), 4, False).tolist() == [[15, 1, 2, 3, 4, 5, 6, 7]]
+
+
+def _gptq_pack(codes, bits):
+    """[N, K] codes -> GPTQ qweight [K/pf, N], with explicit loops."""
+    N, K = codes.shape
+    pf = 32 // bits
+    out = np.zeros((K // pf, N), dtype=np.int64)
+    for n in range(N):
+        for k in range(K):
+            out[k // pf, n] |= int(codes[n, k]) << (bits * (k % pf))
+    return out
+
+
+def _awq_pack(vals):
+    """[R, N] 4-bit values -> AWQ words [R, N/8], with explicit loops."""
+    R, N = vals.shape
+    out = np.zeros((R, N // 8), dtype=np.int64)
+    for r in range(R):
+        for c in range(N // 8):
+            for i in range(8):
+                out[r, c] |= int(vals[r, 8 * c + oracle.AWQ_PACK_ORDER[i]]) << (4 * i)
+    return out
+
+
+@pytest.mark.parametrize("fmt,bits", [("gptq", 4), ("gptq", 8), ("awq", 4)])
+def test_checkpoint_formats_dequantize_like_the_plain_layout(fmt, bits):
+    # the same codes, zero points and scales in a checkpoint layout and in the
+    # plain layout give the same float64 weights
+    rng = np.random.default_rng(bits)
+    N, K, G = 32, 64, 32
+    codes = rng.integers(0, 1 << bits, size=(N, K))
+    zeros = rng.integers(0, 1 << bits, size=(K // G, N))
+    s = halfbits((torch.rand(K // G, N) * 0.01 + 0.001).half())
+    plain = oracle.dequantize_expert(pack_along_last(torch.as_tensor(codes), bits).numpy(), s,
+                                     pack_along_last(torch.as_tensor(zeros), bits).numpy(), bits, G, "f16")
+    if fmt == "gptq":
+        u = oracle.unpack_gptq_qweight(_gptq_pack(codes, bits), bits)
+        zw = np.zeros((K // G, N * bits // 32), dtype=np.int64)
+        for g in range(K // G):
+            for n in range(N):
+                zw[g, n * bits // 32] |= ((int(zeros[g, n]) - 1) % (1 << bits)) << (bits * (n % (32 // bits)))
+        z = oracle.unpack_gptq_qzeros(zw, bits)
+    else:
+        u = oracle.unpack_awq(_awq_pack(codes.T)).T  # AWQ packs [K, N] along N
+        z = oracle.unpack_awq(_awq_pack(zeros))
+    sf = oracle.halfbits_to_f64(s, "f16")
+    g_of_k = np.arange(K) // G
+    W = (u - z.T[:, g_of_k]) * sf.T[:, g_of_k]
+    assert np.array_equal(u, codes) and np.array_equal(z, zeros)
+    assert np.array_equal(W, plain)
