@@ -290,6 +290,30 @@ wna16_status wna16_fused_moe_prepacked(const void* hidden, wna16_dtype act_dtype
                                        void* const* events);
 
 /*
+ * Checkpoint conversion (vLLM PR #12185: the fused kernel's weight format "is
+ * just compatible with gptq/awq" and accepts their weights after a one-off
+ * conversion). The layouts are those of the public packers:
+ *   WNA16_CKPT_GPTQ / _GPTQ_V2: qweight [E, K/pf, N] int32, the codes of
+ *     column n packed along K (LSB first); qzeros [E, K/G, N/pf] packed along
+ *     N, storing z - 1 (GPTQ) or z (GPTQ_V2); bits 4 or 8.
+ *   WNA16_CKPT_AWQ: qweight [E, K, N/8] and qzeros [E, K/G, N/8], 4-bit, packed
+ *     along N with field i of a word holding column 8c + (0 2 4 6 1 3 5 7)[i];
+ *     zero points stored as they are.
+ *   Scales [E, K/G, N] are the library's layout already (no conversion).
+ * Outputs: q_out [E, N, K/pf] and zeros_out [E, K/G, N/pf] in the layout of
+ * this header (qzeros and zeros_out both NULL for symmetric weights). For the
+ * gate/up projection, N = 2I with the gate columns first (concatenate the
+ * checkpoint's gate and up tensors along N before converting). group_size: as
+ * in the layer calls, or -1. Argument errors return before any launch; the
+ * conversion itself cannot fail on the device.
+ */
+typedef enum { WNA16_CKPT_GPTQ = 0, WNA16_CKPT_GPTQ_V2 = 1, WNA16_CKPT_AWQ = 2 } wna16_checkpoint;
+
+wna16_status wna16_convert_checkpoint(wna16_checkpoint format, const int32_t* qweight, const int32_t* qzeros,
+                                      int E, int64_t N, int64_t K, int bits, int group_size, int32_t* q_out,
+                                      int32_t* zeros_out, void* stream);
+
+/*
  * Model variants (vLLM fused_moe/oracle/int8.py: the int8 MoE quant config
  * carries w1_bias / w2_bias, and passes swiglu_alpha / swiglu_beta /
  * swiglu_limit to its clamped-SwiGLU backend; the pages give no formulas, these

@@ -174,3 +174,19 @@ def test_act_order_prepare_errors_are_host_side(lib):
     assert call(q=None, qo=None, perm=None) == 1
     assert call(st=None) == 1
     assert call(perm=v(18)) == 1
+
+
+def test_convert_checkpoint_errors_are_host_side(lib):
+    v = ctypes.c_void_p
+    defaults = (("fmt", 0), ("q", v(16)), ("z", v(16)), ("E", 4), ("N", 256), ("K", 512), ("bits", 4), ("G", 128),
+                ("qo", v(16)), ("zo", v(16)))
+    call = lambda **o: lib.wna16_convert_checkpoint(*[o.get(k, d) for k, d in defaults], None)
+    assert call(fmt=3) == 1
+    assert call(fmt=2, bits=8) == 2  # AWQ is 4-bit
+    assert call(G=0) == 1
+    assert call(G=96) == 2
+    assert call(N=4) == 2  # N must hold whole zero-point words
+    assert call(q=None) == 1
+    assert call(zo=None) == 1  # zeros in, no zeros out
+    assert call(z=None, zo=None, E=0) == 1
+    assert call(qo=v(18)) == 1

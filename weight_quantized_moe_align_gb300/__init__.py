@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     WNA16Error,
     align_capacity,
     choose_block,
+    convert_checkpoint,
     fused_moe,
     fused_moe_noalloc,
     fused_moe_prepacked,

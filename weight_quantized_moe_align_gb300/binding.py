@@ -33,7 +33,7 @@ EXPORTED = (
     "wna16_fused_moe_workspace_bytes", "wna16_fused_moe", "wna16_fused_moe_timed",
     "wna16_fused_moe_noalloc", "wna16_prepack_bytes", "wna16_prepack", "wna16_fused_moe_prepacked",
     "wna16_read_device_status", "wna16_status_string", "wna16_topk_routing", "wna16_fused_moe_ex",
-    "wna16_fused_moe_prepacked_ex", "wna16_act_order_prepare",
+    "wna16_fused_moe_prepacked_ex", "wna16_act_order_prepare", "wna16_convert_checkpoint",
 )
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
@@ -122,6 +122,8 @@ def load() -> ctypes.CDLL:
     L.wna16_fused_moe_ex.restype = i32
     L.wna16_fused_moe_prepacked_ex.argtypes = L.wna16_fused_moe_prepacked.argtypes + [vp]
     L.wna16_fused_moe_prepacked_ex.restype = i32
+    L.wna16_convert_checkpoint.argtypes = [i32, vp, vp, i32, i64, i64, i32, i32, vp, vp, vp]
+    L.wna16_convert_checkpoint.restype = i32
     L.wna16_act_order_prepare.argtypes = [vp, vp, i32, i64, i64, i32, i32, vp, vp, vp, vp, vp]
     L.wna16_act_order_prepare.restype = i32
     L.wna16_topk_routing.argtypes = [vp, i32, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp]
@@ -430,6 +432,37 @@ def act_order_prepare(q: torch.Tensor, g_idx: torch.Tensor, bits: int, group_siz
                                         _ptr(inv), _ptr(status), _stream(stream))
     _raise(st, "wna16_act_order_prepare")
     return q_out, perm, inv
+
+
+_CKPT = {"gptq": 0, "gptq_v2": 1, "awq": 2}
+
+
+def convert_checkpoint(fmt: str, qweight: torch.Tensor, qzeros: Optional[torch.Tensor], bits: int,
+                       group_size: int, stream=None):
+    """GPTQ ("gptq": zeros stored minus one; "gptq_v2") or AWQ ("awq") expert
+    tensors -> (codes [E, N, K/pf], zeros [E, K/G, N/pf] or None) in the layer's
+    layout, by ``wna16_convert_checkpoint``. ``qweight``: GPTQ [E, K/pf, N], AWQ
+    [E, K, N/8]; ``qzeros`` [E, K/G, N/pf] or None. Scales need no conversion."""
+    if fmt not in _CKPT:
+        raise ValueError(f"fmt must be one of {tuple(_CKPT)}")
+    _check(qweight, "qweight", torch.int32)
+    dev = qweight.device
+    pf = 32 // bits
+    if fmt == "awq":
+        E, K, n8 = qweight.shape
+        N = n8 * 8
+    else:
+        E, kw, N = qweight.shape
+        K = kw * pf
+    G = K if group_size == -1 else group_size
+    if qzeros is not None:
+        _check(qzeros, "qzeros", torch.int32, (E, K // G, N // pf), dev)
+    q_out = torch.empty(E, N, K // pf, dtype=torch.int32, device=dev)
+    z_out = None if qzeros is None else torch.empty(E, K // G, N // pf, dtype=torch.int32, device=dev)
+    st = load().wna16_convert_checkpoint(_CKPT[fmt], _ptr(qweight), _ptr(qzeros), E, N, K, bits, group_size,
+                                         _ptr(q_out), _ptr(z_out), _stream(stream))
+    _raise(st, "wna16_convert_checkpoint")
+    return q_out, z_out
 
 
 def read_device_status(status_word: torch.Tensor, stream=None) -> int:
