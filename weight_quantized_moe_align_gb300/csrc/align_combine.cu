@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   __shared__ int total;
   __shared__ int bad;
 
+  grid_dep_launch();  // the gather may start its launch; it waits for this kernel's writes
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid < kMaxExperts) cnt[tid] = 0;
@@ -179,6 +180,8 @@ __global__ void __launch_bounds__(256)
                       const int32_t* __restrict__ slot_of_pair, int P, int topk, int E, int h8, int permute,
                       uint4* __restrict__ x_sorted, float* __restrict__ xs, int cap, float* __restrict__ zero0,
                       int zero_n0, float* __restrict__ zero1, int zero_n1, float* __restrict__ zero2, int zero_n2) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int chunks = h8 / 8;
   const long long n = static_cast<long long>(P) * chunks;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -229,6 +232,8 @@ __global__ void __launch_bounds__(256)
     moe_gather_perm_kernel(const uint16_t* __restrict__ hidden, const int32_t* __restrict__ ids,
                            const int32_t* __restrict__ slot_of_pair, const int32_t* __restrict__ kperm, int P,
                            int topk, int E, int H, int permute, uint4* __restrict__ x_sorted) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int h8 = H / 8;
   const long long n = static_cast<long long>(P) * h8;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -269,6 +274,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     moe_combine_kernel(const float* __restrict__ slab, const int32_t* __restrict__ ids, int M, int H,
                        int topk, int E, int split, T* __restrict__ out) {
+  grid_dep_wait();
   const int h4 = H / 4;
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(M) * h4) return;
@@ -302,7 +308,7 @@ cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, i
 cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
                           int topk, int E, int H, int permute, int act_dtype, int max_ctas, void* x_sorted,
                           float* xs, int cap, float* zero_ptr0, int zero_n0, float* zero_ptr1, int zero_n1,
-                          float* zero_ptr2, int zero_n2, cudaStream_t stream) {
+                          float* zero_ptr2, int zero_n2, cudaStream_t stream, bool pdl) {
   const int h8 = H / 8;
   long long n = static_cast<long long>(P) * (h8 / 8);
   n = std::max<long long>(n, std::max({zero_n0, zero_n1, zero_n2}));
@@ -310,45 +316,35 @@ cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t*
   const long long want = (n + threads - 1) / threads;
   const unsigned blocks = static_cast<unsigned>(want < max_ctas ? want : max_ctas);
   if (blocks == 0) return cudaSuccess;
-  if (act_dtype == 0)
-    moe_gather_kernel<0><<<blocks, threads, 0, stream>>>(static_cast<const uint4*>(hidden), ids, slot_of_pair, P,
-                                                         topk, E, h8, permute, static_cast<uint4*>(x_sorted), xs,
-                                                         cap, zero_ptr0, zero_n0, zero_ptr1, zero_n1, zero_ptr2,
-                                                         zero_n2);
-  else
-    moe_gather_kernel<1><<<blocks, threads, 0, stream>>>(static_cast<const uint4*>(hidden), ids, slot_of_pair, P,
-                                                         topk, E, h8, permute, static_cast<uint4*>(x_sorted), xs,
-                                                         cap, zero_ptr0, zero_n0, zero_ptr1, zero_n1, zero_ptr2,
-                                                         zero_n2);
-  return cudaGetLastError();
+  auto* fn = act_dtype == 0 ? moe_gather_kernel<0> : moe_gather_kernel<1>;
+  return launch_kernel(fn, dim3(blocks), dim3(threads), 0, stream, pdl, static_cast<const uint4*>(hidden), ids,
+                       slot_of_pair, P, topk, E, h8, permute, static_cast<uint4*>(x_sorted), xs, cap, zero_ptr0,
+                       zero_n0, zero_ptr1, zero_n1, zero_ptr2, zero_n2);
 }
 
 cudaError_t launch_gather_perm(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair,
                                const int32_t* kperm, int P, int topk, int E, int H, int permute, int max_ctas,
-                               void* x_sorted, cudaStream_t stream) {
+                               void* x_sorted, cudaStream_t stream, bool pdl) {
   const long long n = static_cast<long long>(P) * (H / 8);
   const int threads = 256;
   const long long want = (n + threads - 1) / threads;
   const unsigned blocks = static_cast<unsigned>(want < max_ctas ? want : max_ctas);
   if (blocks == 0) return cudaSuccess;
-  moe_gather_perm_kernel<<<blocks, threads, 0, stream>>>(static_cast<const uint16_t*>(hidden), ids, slot_of_pair,
-                                                         kperm, P, topk, E, H, permute,
-                                                         static_cast<uint4*>(x_sorted));
-  return cudaGetLastError();
+  return launch_kernel(moe_gather_perm_kernel, dim3(blocks), dim3(threads), 0, stream, pdl,
+                       static_cast<const uint16_t*>(hidden), ids, slot_of_pair, kperm, P, topk, E, H, permute,
+                       static_cast<uint4*>(x_sorted));
 }
 
 cudaError_t launch_combine(const float* slab, const int32_t* ids, int M, int H, int topk, int E,
-                           int split, int act_dtype, void* out, cudaStream_t stream) {
+                           int split, int act_dtype, void* out, cudaStream_t stream, bool pdl) {
   const long long n = static_cast<long long>(M) * (H / 4);
   const int threads = 256;
   const unsigned blocks = static_cast<unsigned>((n + threads - 1) / threads);
   if (act_dtype == 0)
-    moe_combine_kernel<__half><<<blocks, threads, 0, stream>>>(slab, ids, M, H, topk, E, split,
-                                                               static_cast<__half*>(out));
-  else
-    moe_combine_kernel<__nv_bfloat16><<<blocks, threads, 0, stream>>>(
-        slab, ids, M, H, topk, E, split, static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+    return launch_kernel(moe_combine_kernel<__half>, dim3(blocks), dim3(threads), 0, stream, pdl, slab, ids, M, H,
+                         topk, E, split, static_cast<__half*>(out));
+  return launch_kernel(moe_combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, stream, pdl, slab, ids, M,
+                       H, topk, E, split, static_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace wna16

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace wna16 {
 
 // Threads of the grouped-GEMM kernel and their roles (warp index):
@@ -38,6 +40,33 @@ template <int BITS>
 constexpr bool kPermuteK = BITS == 4;
 __host__ __device__ constexpr int permute_k8(int k) {
   return (k & ~7) | ((k & 7) < 4 ? 2 * (k & 7) : 2 * ((k & 7) - 4) + 1);
+}
+
+// Programmatic dependent launch: a kernel launched with pdl = true may start
+// while the previous kernel of the stream still runs. It must call
+// grid_dep_wait() before it touches memory the previous kernels write (the
+// wait returns once they have completed and their writes are visible; without
+// the launch attribute it returns at once). grid_dep_launch() lets the next
+// kernel start once every CTA of this one has issued it or exited, so a
+// waiting dependent never holds resources an unscheduled CTA of its
+// predecessor needs.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 struct GemmArgs {
@@ -76,6 +105,7 @@ struct GemmArgs {
   int glu;                     // gate/up activation: 0 silu(g) * u, 1 clamped SwiGLU
   float glu_alpha, glu_beta, glu_limit;
   const int32_t* act_pos;      // gate/up GEMM, act-order down weights: [E, I] column of feature f in the act cache
+  int pdl;                     // launched as a programmatic dependent of the previous kernel
 };
 
 // One weight stage in shared memory: packed codes of 128 rows x 128 K, then up

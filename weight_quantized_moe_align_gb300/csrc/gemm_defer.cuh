@@ -243,6 +243,9 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // the setup above overlaps the previous kernel; its outputs are read below
+  grid_dep_wait();
+  grid_dep_launch();
 
   int nb = *a.num_post_pad / NT;
   nb = nb < 0 ? 0 : (nb > a.max_blocks ? a.max_blocks : nb);

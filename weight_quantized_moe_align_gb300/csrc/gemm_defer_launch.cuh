@@ -22,8 +22,7 @@ cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t stream, const CUtens
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  fn<<<grid, kDeferThreads, smem, stream>>>(q, s, z, b, x, a);
-  return cudaGetLastError();
+  return launch_kernel(fn, grid, dim3(kDeferThreads), smem, stream, a.pdl != 0, q, s, z, b, x, a);
 }
 
 template <int BITS, int GEMM, int NT, int VAR>

@@ -33,12 +33,12 @@ cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, i
 cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
                           int topk, int E, int H, int permute, int act_dtype, int max_ctas, void* x_sorted,
                           float* xs, int cap, float* zero_ptr0, int zero_n0, float* zero_ptr1, int zero_n1,
-                          float* zero_ptr2, int zero_n2, cudaStream_t stream);
+                          float* zero_ptr2, int zero_n2, cudaStream_t stream, bool pdl);
 // the gather for act-order gate/up weights: x_sorted rows in each expert's K order kperm [E, H]
 cudaError_t launch_gather_perm(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair,
                                const int32_t* kperm, int P, int topk, int E, int H, int permute, int max_ctas,
-                               void* x_sorted, cudaStream_t stream);
+                               void* x_sorted, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(const float* slab, const int32_t* ids, int M, int H, int topk, int E,
-                           int split, int act_dtype, void* out, cudaStream_t stream);
+                           int split, int act_dtype, void* out, cudaStream_t stream, bool pdl);
 
 }  // namespace wna16

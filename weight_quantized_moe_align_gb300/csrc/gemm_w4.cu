@@ -21,8 +21,7 @@ cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t stream, const CUtens
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  fn<<<grid, gemm_threads(LEAN), smem, stream>>>(q, s, z, b, a);
-  return cudaGetLastError();
+  return launch_kernel(fn, grid, dim3(gemm_threads(LEAN)), smem, stream, a.pdl != 0, q, s, z, b, a);
 }
 
 template <int GEMM, int LEAN>

@@ -455,6 +455,10 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   float* xs1 = defer ? reinterpret_cast<float*>(ws + L.xs1) : nullptr;
   float* xs2 = defer ? reinterpret_cast<float*>(ws + L.xs2) : nullptr;
 
+  // Launches after the first run as programmatic dependents of the previous one
+  // (their setup overlaps its tail), except when events are recorded between
+  // them for per-kernel timing.
+  const bool pdl = events == nullptr;
   auto mark = [&](int i) {
     if (events && events[i]) return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
     return true;
@@ -498,11 +502,11 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   if (opt && opt->w13_perm) {
     if (!mark(1) || launch_gather_perm(hidden, topk_ids, slot_of_pair, opt->w13_perm, P, topk, E,
                                        static_cast<int>(H), bits == 4 ? 1 : 0, sm_count() * 8, x_sorted,
-                                       s) != cudaSuccess)
+                                       s, pdl) != cudaSuccess)
       return WNA16_ERR_CUDA;
   } else if (!mark(1) || launch_gather(hidden, topk_ids, slot_of_pair, P, topk, E, static_cast<int>(H), bits == 4 ? 1 : 0,
                                 act_dtype, sm_count() * 8, x_sorted, xs1, static_cast<int>(cap), zero1, zero1_n,
-                                zero2, zero2_n, reinterpret_cast<float*>(cnt1), cnt1_n, s) != cudaSuccess)
+                                zero2, zero2_n, reinterpret_cast<float*>(cnt1), cnt1_n, s, pdl) != cudaSuccess)
     return WNA16_ERR_CUDA;
 
   const Pipe pipe = pipe_for(bits, B);
@@ -544,6 +548,7 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   a1.glu_beta = opt ? opt->swiglu_beta : 0.f;
   a1.glu_limit = opt ? opt->swiglu_limit : 0.f;
   a1.act_pos = opt ? opt->w2_inv_perm : nullptr;
+  a1.pdl = pdl ? 1 : 0;
   a1.wpack = packed ? static_cast<const uint8_t*>(w13_pack) : nullptr;
   a1.wimg = prepack_image_bytes(bits, prepack_sg(r.G1), zeros ? 1 : 0);
   const int64_t units1 = static_cast<int64_t>(max_blocks) * a1.n_tiles * split1;
@@ -588,7 +593,7 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   if (e2 != cudaSuccess) return WNA16_ERR_CUDA;
 
   if (!mark(4) || launch_combine(slab, topk_ids, static_cast<int>(M), static_cast<int>(H), topk, E, r.split,
-                                 act_dtype, out, s) != cudaSuccess)
+                                 act_dtype, out, s, pdl) != cudaSuccess)
     return WNA16_ERR_CUDA;
   if (!mark(5)) return WNA16_ERR_CUDA;
   return WNA16_OK;
