@@ -243,11 +243,11 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // the setup above overlaps the previous kernel; its outputs are read below
-  grid_dep_wait();
-  grid_dep_launch();
-
-  int nb = *a.num_post_pad / NT;
+  // The setup above overlaps the previous kernel. The align kernel's outputs
+  // (block count, expert of each block) were complete before the previous
+  // kernel started: read from L2 without waiting. Everything the previous
+  // kernel writes is read after grid_dep_wait().
+  int nb = __ldcg(a.num_post_pad) / NT;
   nb = nb < 0 ? 0 : (nb > a.max_blocks ? a.max_blocks : nb);
   const int units = nb * a.n_tiles * a.split;
 
@@ -262,38 +262,68 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     // stages per quantization group: G is a multiple of 128, or the whole K
     // (per-channel scales, one group), where rounding up keeps every stage in it
     const int spg = (a.G + kTileK - 1) / kTileK;
+    // weight part of a stage: codes, scales, zero points (no dependence on the
+    // previous kernel) / token part: the token tile and its sums (written by it)
+    auto load_weights = [&](int s, const Unit& w, int e, int kt, int ys) {
+      uint8_t* dst = wring + s * WST;
+      if (a.wpack) {
+        // prepacked: the stage's codes, scales and zero points as one image
+        const uint8_t* src = a.wpack + ((static_cast<size_t>(e) * a.n_tiles + w.tile) * a.kt_total + kt) * a.wimg;
+        bulk_load(dst, src, a.wimg, &full[s], pol_w);
+      } else if (GEMM == 1) {
+        const int f0 = w.tile * kGateUpRows;
+        tma_load_3d(dst, &tm_q, &full[s], kt * KW, f0, 2 * e, pol_w);
+        tma_load_3d(dst + S_OFF, &tm_s, &full[s], f0, 0, ys, pol_w);
+        if (a.has_zeros) tma_load_3d(dst + Z_OFF, &tm_z, &full[s], f0 / PF, 0, ys, pol_w);
+      } else {
+        const int r0 = w.tile * kTileRows;
+        tma_load_2d(dst, &tm_q, &full[s], kt * KW, e * a.N + r0, pol_w);
+        tma_load_2d(dst + S_OFF, &tm_s, &full[s], r0, ys, pol_w);
+        if (a.has_zeros) tma_load_2d(dst + Z_OFF, &tm_z, &full[s], r0 / PF, ys, pol_w);
+      }
+    };
+    auto load_tokens = [&](int s, const Unit& w, int kt) {
+#pragma unroll
+      for (int c = 0; c < kTileK / kChunkK; ++c)
+        tma_load_2d(bring + s * BST + c * NT * 128, &tm_b, &full[s], kt * kTileK + c * kChunkK, w.blk * NT, pol_b);
+      tma_load_3d(xring + s * (XST / 4), &tm_x, &full[s], w.blk * NT, 0, kt, pol_b);
+    };
+    // The first ring's worth of weight stages is requested before waiting for
+    // the previous kernel (its slots are fresh); their token parts follow the
+    // wait, in the main loop.
+    int pre = 0;
+    for (int u = blockIdx.x; u < units && pre < NS; u += gridDim.x) {
+      const Unit w = decode_unit(u, nb, a);
+      const int e = unit_expert_l2(a, w.blk);
+      int ys = e * a.groups + w.kt0 / spg, gk = w.kt0 % spg;
+      for (int kt = w.kt0; kt < w.kt1 && pre < NS; ++kt, ++pre) {
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&full[pre], stage_tx);
+          load_weights(pre, w, e, kt, ys);
+        }
+        __syncwarp();
+        if (++gk == spg) {
+          gk = 0;
+          ++ys;
+        }
+      }
+    }
+    grid_dep_wait();
+    grid_dep_launch();
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = decode_unit(u, nb, a);
-      const int e = unit_expert(a, w.blk);
+      const int e = unit_expert_l2(a, w.blk);
       // scale / zero-point row of the current stage, advanced per group
       int ys = e * a.groups + w.kt0 / spg, gk = w.kt0 % spg;
       bool ok = true;
       for (int kt = w.kt0; kt < w.kt1; ++kt, ++it) {
-        if (!warp_wait_all(&empty[s], e_phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
+        if (it >= pre && !warp_wait_all(&empty[s], e_phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
         if (elect_one()) {
-          mbar_arrive_expect_tx(&full[s], stage_tx);
-          uint8_t* dst = wring + s * WST;
-          if (a.wpack) {
-            // prepacked: the stage's codes, scales and zero points as one image
-            const uint8_t* src =
-                a.wpack + ((static_cast<size_t>(e) * a.n_tiles + w.tile) * a.kt_total + kt) * a.wimg;
-            bulk_load(dst, src, a.wimg, &full[s], pol_w);
-          } else if (GEMM == 1) {
-            const int f0 = w.tile * kGateUpRows;
-            tma_load_3d(dst, &tm_q, &full[s], kt * KW, f0, 2 * e, pol_w);
-            tma_load_3d(dst + S_OFF, &tm_s, &full[s], f0, 0, ys, pol_w);
-            if (a.has_zeros) tma_load_3d(dst + Z_OFF, &tm_z, &full[s], f0 / PF, 0, ys, pol_w);
-          } else {
-            const int r0 = w.tile * kTileRows;
-            tma_load_2d(dst, &tm_q, &full[s], kt * KW, e * a.N + r0, pol_w);
-            tma_load_2d(dst + S_OFF, &tm_s, &full[s], r0, ys, pol_w);
-            if (a.has_zeros) tma_load_2d(dst + Z_OFF, &tm_z, &full[s], r0 / PF, ys, pol_w);
+          if (it >= pre) {
+            mbar_arrive_expect_tx(&full[s], stage_tx);
+            load_weights(s, w, e, kt, ys);
           }
-#pragma unroll
-          for (int c = 0; c < kTileK / kChunkK; ++c)
-            tma_load_2d(bring + s * BST + c * NT * 128, &tm_b, &full[s], kt * kTileK + c * kChunkK, w.blk * NT,
-                        pol_b);
-          tma_load_3d(xring + s * (XST / 4), &tm_x, &full[s], w.blk * NT, 0, kt, pol_b);
+          load_tokens(s, w, kt);
         }
         __syncwarp();
         if (++s == NS) {
@@ -310,6 +340,8 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     for (int j = (it > NS ? it - NS : 0); j < it; ++j) wait_bar_drain(&full[j % NS], (j / NS) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    grid_dep_wait();
+    grid_dep_launch();
     const uint32_t idesc = idesc_f16(ACT, NT);
     const uint64_t chunk_step = static_cast<uint64_t>((NT * 128) >> 4);
     const uint64_t bc0 = smem_desc_sw128(smem_u32(bcorr));
@@ -353,6 +385,8 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     }
   } else {
     // ------------------------------------------------------------ dequant warpgroups
+    grid_dep_wait();
+    grid_dep_launch();
     const int g = (warp - 2) >> 2;
     const int q = warp & 3;  // TMEM lane quarter
     int srow, half = 0, hrow;

@@ -205,6 +205,13 @@ __device__ __forceinline__ int unit_expert(const GemmArgs& a, int blk) {
   return (e >= 0 && e < a.E) ? e : 0;  // blocks below num_post_pad always hold a valid id
 }
 
+// The same read from L2 (the align kernel's output, read by a kernel that may
+// have started before its predecessor finished).
+__device__ __forceinline__ int unit_expert_l2(const GemmArgs& a, int blk) {
+  const int e = __ldcg(a.expert_ids + blk);
+  return (e >= 0 && e < a.E) ? e : 0;
+}
+
 // Epilogue of one work unit, run by four warps covering the four TMEM lane
 // quarters: waits for the unit's accumulator, reads it 16 token columns at a
 // time and writes silu(gate) * up to the act cache (gate/up GEMM) or the
