@@ -226,19 +226,18 @@ def time_oracle(li, target_s, max_tokens=1):
 
     wl = li.wl
     unit = 64 if wl.group_size == -1 else max(64, wl.group_size)
-    F = unit
-    t0 = time.perf_counter()
-    oracle.fused_moe_grouped(sample_layer(li, 1, F))
-    dt = max(time.perf_counter() - t0, 1e-4)
-    scale = target_s / dt
-    F = int(min(wl.I, max(unit, int(F * scale) // unit * unit)))
-    tokens = 1
-    if F == wl.I:
-        tokens = int(max(1, min(max_tokens, scale * unit / wl.I)))
-    L = sample_layer(li, tokens, F)
-    t0 = time.perf_counter()
-    oracle.fused_moe_grouped(L)
-    dt = time.perf_counter() - t0
+    oracle.fused_moe_grouped(sample_layer(li, 1, unit))  # untimed: first-call and thread start-up costs
+    F, tokens, dt = unit, 1, 0.0
+    for _ in range(3):  # size the sample from the last timing, up to three rounds
+        t0 = time.perf_counter()
+        oracle.fused_moe_grouped(sample_layer(li, tokens, F))
+        dt = max(time.perf_counter() - t0, 1e-4)
+        if dt >= 0.5 * target_s or (F == wl.I and tokens >= max_tokens):
+            break
+        scale = target_s / dt
+        work = tokens * F * scale  # token-features the target allows
+        F = int(min(wl.I, max(unit, int(work) // unit * unit)))
+        tokens = int(max(1, min(max_tokens, work // wl.I))) if F == wl.I else 1
     desc = (f"first {tokens} token(s) x first {F} of I={wl.I} intermediate features of each routed expert "
             f"(work {tokens * F / wl.I:.4f} tokens)")
     return tokens * F / wl.I / dt, desc, dt
