@@ -172,8 +172,9 @@ __device__ __forceinline__ float scale_to_f32(uint32_t bits) {
   else return __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(bits)));
 }
 
-// VAR = 1: the model-variant epilogues (biases, clamped SwiGLU), a separate
-// instantiation so that the default one keeps its register allocation.
+// VAR = 1: prepacked weights and the model-variant epilogues (biases, clamped
+// SwiGLU), a separate instantiation so that the default one keeps its
+// register allocation.
 template <int BITS, int ACT, int SCL, int GEMM, int NT, int VAR>
 __global__ void __launch_bounds__(kDeferThreads, 2)
     moe_gemm_defer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    if (!a.wpack) {
+    if (!(VAR && a.wpack)) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_s);
       if (a.has_zeros) prefetch_tmap(&tm_z);
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     const uint32_t stage_tx =
-        (a.wpack ? a.wimg : W_BYTES + 256 + (a.has_zeros ? (kTileRows / PF) * 4 : 0)) + BST + XST;
+        ((VAR && a.wpack) ? a.wimg : W_BYTES + 256 + (a.has_zeros ? (kTileRows / PF) * 4 : 0)) + BST + XST;
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_b = l2_policy_evict_last();
     int it = 0, s = 0;
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     // previous kernel) / token part: the token tile and its sums (written by it)
     auto load_weights = [&](int s, const Unit& w, int e, int kt, int ys) {
       uint8_t* dst = wring + s * WST;
-      if (a.wpack) {
+      if (VAR && a.wpack) {
         // prepacked: the stage's codes, scales and zero points as one image
         const uint8_t* src = a.wpack + ((static_cast<size_t>(e) * a.n_tiles + w.tile) * a.kt_total + kt) * a.wimg;
         bulk_load(dst, src, a.wimg, &full[s], pol_w);
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     const int si = GEMM == 1 ? half * kGateUpRows + hrow : hrow;
     const int zi = GEMM == 1 ? half * (kGateUpRows / PF) + hrow / PF : hrow / PF;
     const int zshift = BITS * (hrow % PF);
-    const int z_off = a.wpack ? W_BYTES + 256 : Z_OFF;  // zero points: right after the scales in an image
+    const int z_off = (VAR && a.wpack) ? W_BYTES + 256 : Z_OFF;  // zero points: right after the scales in an image
     const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t a_slot = tmem + t_lane + kDeferA0 + g * kDeferAStride;
     const uint32_t p_addr = tmem + t_lane + g * NT;

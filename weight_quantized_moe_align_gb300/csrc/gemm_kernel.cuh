@@ -217,7 +217,7 @@ __device__ __forceinline__ int unit_expert_l2(const GemmArgs& a, int blk) {
 // time and writes silu(gate) * up to the act cache (gate/up GEMM) or the
 // top-k-weighted fp32 row of each (token, slot) pair (down GEMM), then frees
 // the accumulator. Returns false if the wait gave up.
-template <int BITS, int ACT, int GEMM>
+template <int BITS, int ACT, int GEMM, int EXT>
 __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, uint32_t tmem, int acc,
                                               uint32_t acc_phase, uint64_t* accfull, uint64_t* accempty,
                                               volatile int* abort_flag, int q, int lane) {
@@ -236,13 +236,13 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
   if (GEMM == 1) {
     const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
     int pos = f;
-    if (a.act_pos) {
+    if (EXT && a.act_pos) {
       pos = a.act_pos[static_cast<size_t>(unit_expert(a, w.blk)) * a.I + f];
       fp_ok = static_cast<unsigned>(pos) < static_cast<unsigned>(a.I);
     }
     fp = kPermuteK<BITS> ? permute_k8(pos) : pos;
   }
-  if (a.bias) {
+  if (EXT && a.bias) {
     const int e = unit_expert(a, w.blk);
     if (GEMM == 1) {
       const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
@@ -275,7 +275,7 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
         const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, lo ? v[j + 8] : v[j], 16);
         const float g = __uint_as_float(lo ? mine : other);
         const float up = __uint_as_float(lo ? other : mine);
-        const float val = gate_up_act(a, g, up);
+        const float val = EXT ? gate_up_act(a, g, up) : g / (1.0f + __expf(-g)) * up;
         const int col = c0 + (lo ? j : j + 8);
         const size_t row = static_cast<size_t>(w.blk) * NT + col;
         if (!fp_ok) continue;
@@ -308,7 +308,11 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
 // warpgroups), two CTAs per SM. LEAN = 1: 6 warps (producer, MMA issuer, one
 // dequant warpgroup that also runs the epilogue), four CTAs per SM, so four
 // MMA-issuing threads share the SM's tensor core (decode-sized token tiles).
-template <int BITS, int ACT, int SCL, int GEMM, int LEAN>
+//
+// EXT = 1: the instantiations that also serve prepacked weights, biases, the
+// clamped SwiGLU and act-order; EXT = 0 carries none of that code (the
+// register-bound dequant loop was measurably slower with it).
+template <int BITS, int ACT, int SCL, int GEMM, int LEAN, int EXT>
 __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
                     const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_b,
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    if (!a.wpack) {
+    if (!(EXT && a.wpack)) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_s);
       if (a.has_zeros) prefetch_tmap(&tm_z);
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     // The whole warp runs the loop (waits are warp-wide polls); one elected
     // lane issues the copies.
     const uint32_t stage_tx =
-        (a.wpack ? a.wimg : W_BYTES + SG * 256 + (a.has_zeros ? SG * (kTileRows / PF) * 4 : 0)) + BST;
+        ((EXT && a.wpack) ? a.wimg : W_BYTES + SG * 256 + (a.has_zeros ? SG * (kTileRows / PF) * 4 : 0)) + BST;
     const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
     const uint64_t pol_b = l2_policy_evict_last();   // token rows: re-read by every row tile
     int it = 0, s = 0;
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
           mbar_arrive_expect_tx(&full[s], stage_tx);
           uint8_t* dst = wring + s * WST;
           const int ys = e * a.groups + (kt * kTileK) / a.G;
-          if (a.wpack) {
+          if (EXT && a.wpack) {
             // prepacked: the stage's codes, scales and zero points as one image
             const uint8_t* src =
                 a.wpack + ((static_cast<size_t>(e) * a.n_tiles + w.tile) * a.kt_total + kt) * a.wimg;
@@ -494,7 +498,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     int uc = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
       const Unit w = decode_unit(u, nb, a);
-      if (!epilogue_unit<BITS, ACT, GEMM>(a, w, tmem, uc % NACC, (uc / NACC) & 1, accfull, accempty, abort_flag, q, lane))
+      if (!epilogue_unit<BITS, ACT, GEMM, EXT>(a, w, tmem, uc % NACC, (uc / NACC) & 1, accfull, accempty, abort_flag, q, lane))
         break;
     }
   } else {
@@ -520,7 +524,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
       hrow = srow;
     }
     const uint32_t t_lane = (q * 32) << 16;
-    const int z_off = a.wpack ? W_BYTES + SG * 256 : Z_OFF;  // zero points: right after the scales in an image
+    const int z_off = (EXT && a.wpack) ? W_BYTES + SG * 256 : Z_OFF;  // zero points: right after the scales in an image
     // This group's stages are the running stage indices gi = grp, grp + step,
     // ... across units (step 2, or 1 for LEAN). Tracked incrementally: the ring
     // slot cs and phase cf of stage gi, its A slot cslot, and the ring slot cps
@@ -599,7 +603,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
       if (!ok) break;
       if (LEAN) {
         // this warpgroup also runs the epilogue, right after the unit's last stage
-        if (!epilogue_unit<BITS, ACT, GEMM>(a, w, tmem, uc % NACC, (uc / NACC) & 1, accfull, accempty, abort_flag, q,
+        if (!epilogue_unit<BITS, ACT, GEMM, EXT>(a, w, tmem, uc % NACC, (uc / NACC) & 1, accfull, accempty, abort_flag, q,
                                       lane))
           break;
         ++uc;

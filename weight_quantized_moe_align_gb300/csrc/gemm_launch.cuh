@@ -18,7 +18,7 @@ bool defer_supported(int bits, int act);
 cudaError_t launch_gemm_defer(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
                               const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                               const CUtensorMap& b, const CUtensorMap& x, const GemmArgs& a);
-// the same with the model-variant epilogues (a.bias or a.glu set)
+// the same for prepacked weights or the model-variant epilogues (a.wpack, a.bias or a.glu set)
 cudaError_t launch_gemm_defer_var(int bits, int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
                               const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                               const CUtensorMap& b, const CUtensorMap& x, const GemmArgs& a);

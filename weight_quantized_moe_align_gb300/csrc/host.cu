@@ -457,8 +457,10 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
 
   // Launches after the first run as programmatic dependents of the previous one
   // (their setup overlaps its tail), except when events are recorded between
-  // them for per-kernel timing.
-  const bool pdl = events == nullptr;
+  // them for per-kernel timing, and for batches past 8192 routed pairs: on one
+  // GB300 the overlap saved 24% of the layer at 2 pairs and 0.6% at 8192, and
+  // cost 2% at 16384 (int8 Mixtral-8x22B shapes).
+  const bool pdl = events == nullptr && P <= 8192;
   auto mark = [&](int i) {
     if (events && events[i]) return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
     return true;
