@@ -272,6 +272,19 @@ def workload_label(wl, M):
             f"{wl.act_dtype} act, {wl.scale_dtype} scales, M={M}")
 
 
+def aggregate_ranks(total_ms, M, steps, dist=None, device="cpu"):
+    """Whole-job figures of a replicas run: every rank processed M tokens per step
+    for `steps` steps; the job took the longest rank's time. Returns
+    (max total ms over ranks, tokens/s of all ranks together)."""
+    world = 1
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, world * M * steps / (total_ms / 1000.0)
+
+
 def reference_arm(args):
     """The oracle as it stands, on the host cores, on a bounded sample per step."""
     rank = int(os.environ.get("RANK", "0"))
@@ -403,12 +416,8 @@ def ours_arm(args):
     total_ms = float(step_ms.sum())
     # ---- per-kernel breakdown (dominant kernel for the roofline), same steps count
     per = timed(call, args.steps, 3)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = aggregate_ranks(total_ms, M, args.steps, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * M * args.steps / (total_ms / 1000.0)
 
     ids_np = li.topk_ids.cpu().numpy()
     alg = algorithmic(wl, M, ids_np)
