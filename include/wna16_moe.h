@@ -337,6 +337,14 @@ wna16_status wna16_convert_checkpoint(wna16_checkpoint format, const int32_t* qw
  *             With either permutation the layer runs the general GEMM kernel
  *             (the 16-token deferred-scale kernel needs contiguous feature
  *             runs). Out-of-range entries are skipped, never dereferenced.
+ *   router_logits [M, E] (logits_dtype) or NULL: route on the device first.
+ *             The call runs wna16_topk_routing (scoring, renormalize,
+ *             n_groups, topk_groups as there) into routed_ids [M, topk] int32
+ *             and routed_weights [M, topk] fp32 (both required, written), then
+ *             the layer on them; the topk_ids / topk_weights arguments are then
+ *             ignored and may be NULL. Routing argument errors return before
+ *             any launch; the routing launch precedes the five of the layer (the
+ *             timed variant's events cover the layer's five).
  * A zero-initialized struct (or a NULL pointer) is the default layer. Both
  * bias pointers must be aligned to their 2-byte elements, the permutations to
  * 4 bytes.
@@ -352,6 +360,14 @@ typedef struct {
   float swiglu_limit;
   const int32_t* w13_perm;
   const int32_t* w2_inv_perm;
+  const void* router_logits;
+  wna16_dtype logits_dtype;
+  wna16_scoring scoring;
+  int renormalize;
+  int n_groups;
+  int topk_groups;
+  int32_t* routed_ids;
+  float* routed_weights;
 } wna16_moe_options;
 
 /*

@@ -135,7 +135,10 @@ def test_routing_argument_errors_are_host_side(lib):
 class _Opt(ctypes.Structure):
     _fields_ = [("w13_bias", ctypes.c_void_p), ("w2_bias", ctypes.c_void_p), ("activation", ctypes.c_int),
                 ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
-                ("swiglu_limit", ctypes.c_float), ("w13_perm", ctypes.c_void_p), ("w2_inv_perm", ctypes.c_void_p)]
+                ("swiglu_limit", ctypes.c_float), ("w13_perm", ctypes.c_void_p), ("w2_inv_perm", ctypes.c_void_p),
+                ("router_logits", ctypes.c_void_p), ("logits_dtype", ctypes.c_int), ("scoring", ctypes.c_int),
+                ("renormalize", ctypes.c_int), ("n_groups", ctypes.c_int), ("topk_groups", ctypes.c_int),
+                ("routed_ids", ctypes.c_void_p), ("routed_weights", ctypes.c_void_p)]
 
 
 def _call_fused_ex(lib, opt):
@@ -154,6 +157,10 @@ def test_options_errors_are_host_side(lib):
     assert _call_fused_ex(lib, _Opt(None, None, 1, 1.7, 1.0, nan)) == 1
     assert _call_fused_ex(lib, _Opt(None, None, 0, 1.0, 0.0, 0.0, 18, None)) == 1  # misaligned permutation
     assert _call_fused_ex(lib, _Opt(None, None, 0, 1.0, 0.0, 0.0, None, 34)) == 1
+    # routing from logits: output buffers required; bad routing arguments before any launch
+    assert _call_fused_ex(lib, _Opt(None, None, 0, 1.0, 0.0, 0.0, None, None, 16, 2, 0, 1, 1, 1, None, 16)) == 1
+    assert _call_fused_ex(lib, _Opt(None, None, 0, 1.0, 0.0, 0.0, None, None, 16, 2, 5, 1, 1, 1, 16, 16)) == 1
+    assert _call_fused_ex(lib, _Opt(None, None, 0, 1.0, 0.0, 0.0, None, None, 16, 2, 0, 1, 3, 1, 16, 16)) == 1
     v = ctypes.c_void_p
     # M = 0 with valid options: OK, nothing launched
     assert lib.wna16_fused_moe_ex(v(16), 0, 0, 256, 512, 8, 2, v(16), v(16), None, v(16), v(16), None, 0, 4, 128,

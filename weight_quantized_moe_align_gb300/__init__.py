@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     fused_moe,
     fused_moe_noalloc,
     fused_moe_prepacked,
+    fused_moe_routed,
     load,
     moe_align_block_size,
     prepack,

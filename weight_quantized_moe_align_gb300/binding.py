@@ -45,7 +45,10 @@ class MoeOptions(ctypes.Structure):
     """``wna16_moe_options``: biases and the gate/up activation."""
     _fields_ = [("w13_bias", ctypes.c_void_p), ("w2_bias", ctypes.c_void_p), ("activation", ctypes.c_int),
                 ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
-                ("swiglu_limit", ctypes.c_float), ("w13_perm", ctypes.c_void_p), ("w2_inv_perm", ctypes.c_void_p)]
+                ("swiglu_limit", ctypes.c_float), ("w13_perm", ctypes.c_void_p), ("w2_inv_perm", ctypes.c_void_p),
+                ("router_logits", ctypes.c_void_p), ("logits_dtype", ctypes.c_int), ("scoring", ctypes.c_int),
+                ("renormalize", ctypes.c_int), ("n_groups", ctypes.c_int), ("topk_groups", ctypes.c_int),
+                ("routed_ids", ctypes.c_void_p), ("routed_weights", ctypes.c_void_p)]
 
 
 _ACTIVATION = {"silu": 0, "swiglu_clamp": 1}
@@ -301,6 +304,71 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
         st = load().wna16_fused_moe_timed(*args, arr)
     _raise(st, "wna16_fused_moe")
     return out
+
+
+def fused_moe_routed(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tensor,
+                     w13_zeros: Optional[torch.Tensor], w2_q: torch.Tensor, w2_scales: torch.Tensor,
+                     w2_zeros: Optional[torch.Tensor], router_logits: torch.Tensor, topk: int, bits: int,
+                     group_size: int, scoring: str = "softmax", renormalize: bool = True, n_groups: int = 1,
+                     topk_groups: int = 1, out: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, block: int = 0, split_k: int = 0, stream=None,
+                     topk_ids: Optional[torch.Tensor] = None, topk_weights: Optional[torch.Tensor] = None,
+                     **variants):
+    """The layer from router logits in one library call (``wna16_fused_moe_ex``
+    with ``router_logits``): top-k routing on the device, then the layer.
+    Returns (out [M, H], topk_ids [M, topk], topk_weights [M, topk]); the last two
+    are written by the call. ``variants``: the keyword options of
+    :func:`fused_moe` (biases, SwiGLU, act-order permutations)."""
+    _check(hidden, "hidden", (torch.float16, torch.bfloat16))
+    _check(router_logits, "router_logits", tuple(_LOGIT_DTYPE))
+    if scoring not in _SCORING:
+        raise ValueError(f"scoring must be one of {tuple(_SCORING)}")
+    dev = hidden.device
+    M, H = hidden.shape
+    E, twoI, _ = w13_q.shape
+    I = twoI // 2
+    _check(router_logits, "router_logits", device=dev, shape=(M, E))
+    if topk_ids is None:
+        topk_ids = torch.empty(M, topk, dtype=torch.int32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty(M, topk, dtype=torch.float32, device=dev)
+    _check(topk_ids, "topk_ids", torch.int32, (M, topk), dev)
+    _check(topk_weights, "topk_weights", torch.float32, (M, topk), dev)
+    if out is None:
+        out = torch.empty_like(hidden)
+    _check(out, "out", hidden.dtype, (M, H), dev)
+    pf = 32 // bits
+    G1 = H if group_size == -1 else group_size
+    G2 = I if group_size == -1 else group_size
+    _check(w13_q, "w13_q", torch.int32, (E, 2 * I, H // pf), dev)
+    _check(w2_q, "w2_q", torch.int32, (E, H, I // pf), dev)
+    _check(w13_scales, "w13_scales", (torch.float16, torch.bfloat16), (E, H // G1, 2 * I), dev)
+    _check(w2_scales, "w2_scales", w13_scales.dtype, (E, I // G2, H), dev)
+    need = workspace_bytes(M, H, I, E, topk, bits, group_size, block, split_k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", torch.uint8, device=dev)
+    opt = _options(hidden, E, I, H, variants.pop("w13_bias", None), variants.pop("w2_bias", None),
+                   variants.pop("activation", "silu"), variants.pop("swiglu", (1.702, 1.0, 7.0)),
+                   variants.pop("w13_perm", None), variants.pop("w2_inv_perm", None))
+    if variants:
+        raise TypeError(f"unexpected options {sorted(variants)}")
+    if opt is None:
+        opt = MoeOptions(None, None, 0, 1.0, 0.0, 0.0, None, None)
+    opt.router_logits = router_logits.data_ptr()
+    opt.logits_dtype = _LOGIT_DTYPE[router_logits.dtype]
+    opt.scoring = _SCORING[scoring]
+    opt.renormalize = int(bool(renormalize))
+    opt.n_groups = n_groups
+    opt.topk_groups = topk_groups
+    opt.routed_ids = topk_ids.data_ptr()
+    opt.routed_weights = topk_weights.data_ptr()
+    st = load().wna16_fused_moe_ex(
+        _ptr(hidden), _DTYPE[hidden.dtype], M, H, I, E, topk, _ptr(w13_q), _ptr(w13_scales), _ptr(w13_zeros),
+        _ptr(w2_q), _ptr(w2_scales), _ptr(w2_zeros), _DTYPE[w13_scales.dtype], bits, group_size, None, None,
+        _ptr(out), _ptr(workspace), workspace.numel(), block, split_k, _stream(stream), None, ctypes.byref(opt))
+    _raise(st, "wna16_fused_moe_ex")
+    return out, topk_ids, topk_weights
 
 
 def fused_moe_noalloc(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tensor,

@@ -2,6 +2,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "wna16_moe.h"
 
 namespace wna16 {
 
@@ -38,6 +39,10 @@ cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t*
 cudaError_t launch_gather_perm(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair,
                                const int32_t* kperm, int P, int topk, int E, int H, int permute, int max_ctas,
                                void* x_sorted, cudaStream_t stream, bool pdl);
+// argument checks of wna16_topk_routing, without any CUDA call
+wna16_status routing_check(const void* logits, wna16_dtype logits_dtype, int64_t M, int E, int topk,
+                           wna16_scoring scoring, int n_groups, int topk_groups, const int32_t* topk_ids,
+                           const float* topk_weights);
 cudaError_t launch_combine(const float* slab, const int32_t* ids, int M, int H, int topk, int E,
                            int split, int act_dtype, void* out, cudaStream_t stream, bool pdl);
 

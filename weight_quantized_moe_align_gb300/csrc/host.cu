@@ -409,6 +409,15 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   const wna16_status st = resolve(M, H, I, E, topk, bits, group_size, block, split_k, &r);
   if (st != WNA16_OK) return st;
   if (M == 0) return WNA16_OK;
+  // routing on the device first: the layer runs on the ids and weights it writes
+  const bool routed = opt && opt->router_logits;
+  if (routed) {
+    const wna16_status rs = routing_check(opt->router_logits, opt->logits_dtype, M, E, topk, opt->scoring,
+                                          opt->n_groups, opt->topk_groups, opt->routed_ids, opt->routed_weights);
+    if (rs != WNA16_OK) return rs;
+    topk_ids = opt->routed_ids;
+    topk_weights = opt->routed_weights;
+  }
   const bool packed = w13_pack != nullptr || w2_pack != nullptr;
   if (!hidden || !topk_ids || !topk_weights || !out || !workspace) return WNA16_ERR_INVALID_ARG;
   if (packed) {
@@ -481,6 +490,13 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
                 !make_xs_map(&x2, xs2, cap, defer_xs_parts(2), kt2, B)))
     return WNA16_ERR_CUDA;
 
+  if (routed) {
+    // its own argument checks run before its launch, the first of this call
+    const wna16_status rs = wna16_topk_routing(opt->router_logits, opt->logits_dtype, M, E, topk, opt->scoring,
+                                               opt->renormalize, opt->n_groups, opt->topk_groups, opt->routed_ids,
+                                               opt->routed_weights, stream);
+    if (rs != WNA16_OK) return rs;
+  }
   if (!mark(0) || launch_align(topk_ids, P, E, B, static_cast<int>(cap), sorted, experts, npp, counts, status,
                                slot_of_pair, s) != cudaSuccess)
     return WNA16_ERR_CUDA;

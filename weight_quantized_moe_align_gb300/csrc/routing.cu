@@ -210,9 +210,12 @@ void launch_routing(const void* logits, const RouteArgs& a, cudaStream_t s) {
 
 using namespace wna16;
 
-extern "C" wna16_status wna16_topk_routing(const void* logits, wna16_dtype logits_dtype, int64_t M, int E,
-                                           int topk, wna16_scoring scoring, int renormalize, int n_groups,
-                                           int topk_groups, int32_t* topk_ids, float* topk_weights, void* stream) {
+namespace wna16 {
+
+// Host-side argument checks of the routing call (no CUDA call).
+wna16_status routing_check(const void* logits, wna16_dtype logits_dtype, int64_t M, int E, int topk,
+                           wna16_scoring scoring, int n_groups, int topk_groups, const int32_t* topk_ids,
+                           const float* topk_weights) {
   if (M < 0 || M >= (int64_t(1) << 31) || E < 1 || E > 256 || topk < 1 || topk > 32 || topk > E)
     return WNA16_ERR_INVALID_ARG;
   if (scoring != WNA16_SCORE_SOFTMAX && scoring != WNA16_SCORE_SIGMOID) return WNA16_ERR_INVALID_ARG;
@@ -230,6 +233,17 @@ extern "C" wna16_status wna16_topk_routing(const void* logits, wna16_dtype logit
   if ((reinterpret_cast<uintptr_t>(logits) % esz) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
       (reinterpret_cast<uintptr_t>(topk_weights) & 3u))
     return WNA16_ERR_INVALID_ARG;
+  return WNA16_OK;
+}
+
+}  // namespace wna16
+
+extern "C" wna16_status wna16_topk_routing(const void* logits, wna16_dtype logits_dtype, int64_t M, int E,
+                                           int topk, wna16_scoring scoring, int renormalize, int n_groups,
+                                           int topk_groups, int32_t* topk_ids, float* topk_weights, void* stream) {
+  const wna16_status st =
+      routing_check(logits, logits_dtype, M, E, topk, scoring, n_groups, topk_groups, topk_ids, topk_weights);
+  if (st != WNA16_OK || M == 0) return st;
   RouteArgs a{static_cast<int>(M), E, topk, scoring == WNA16_SCORE_SIGMOID ? 1 : 0, renormalize ? 1 : 0,
               n_groups, n_groups > 1 ? topk_groups : 1, topk_ids, topk_weights};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
