@@ -425,6 +425,17 @@ wna16_status wna16_fused_moe_prepacked_ex(const void* hidden, wna16_dtype act_dt
  */
 wna16_status wna16_read_device_status(const void* status_word, int32_t* bits_out, void* stream);
 
+/*
+ * Failure-path self-check (diagnostics and tests): launches one CTA whose warps
+ * wait, with the pipelines' own bounded wait, on barriers that nothing
+ * completes. After the bound (about 2 s) the wait gives up, or-s
+ * WNA16_DEV_TIMEOUT into *device_status (not reset here), and the CTA's other
+ * waiting warp leaves through the abort flag; each waiting warp that left adds
+ * 1 to *roles_left (optional, 2 when both did). Tensor memory the CTA held is
+ * freed and the context stays usable. Asynchronous on `stream`.
+ */
+wna16_status wna16_check_wait_timeout(int32_t* device_status, int32_t* roles_left, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* wna16_status_string(wna16_status status);
 

@@ -34,6 +34,7 @@ EXPORTED = (
     "wna16_fused_moe_noalloc", "wna16_prepack_bytes", "wna16_prepack", "wna16_fused_moe_prepacked",
     "wna16_read_device_status", "wna16_status_string", "wna16_topk_routing", "wna16_fused_moe_ex",
     "wna16_fused_moe_prepacked_ex", "wna16_act_order_prepare", "wna16_convert_checkpoint",
+    "wna16_check_wait_timeout",
 )
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
@@ -125,6 +126,8 @@ def load() -> ctypes.CDLL:
     L.wna16_fused_moe_ex.restype = i32
     L.wna16_fused_moe_prepacked_ex.argtypes = L.wna16_fused_moe_prepacked.argtypes + [vp]
     L.wna16_fused_moe_prepacked_ex.restype = i32
+    L.wna16_check_wait_timeout.argtypes = [vp, vp, vp]
+    L.wna16_check_wait_timeout.restype = i32
     L.wna16_convert_checkpoint.argtypes = [i32, vp, vp, i32, i64, i64, i32, i32, vp, vp, vp]
     L.wna16_convert_checkpoint.restype = i32
     L.wna16_act_order_prepare.argtypes = [vp, vp, i32, i64, i64, i32, i32, vp, vp, vp, vp, vp]
@@ -531,6 +534,17 @@ def convert_checkpoint(fmt: str, qweight: torch.Tensor, qzeros: Optional[torch.T
                                          _ptr(q_out), _ptr(z_out), _stream(stream))
     _raise(st, "wna16_convert_checkpoint")
     return q_out, z_out
+
+
+def check_wait_timeout(status: torch.Tensor, roles_left: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Runs the bounded-wait failure path on purpose (``wna16_check_wait_timeout``):
+    about 2 s later ``status`` (int32 [1]) holds DEV_TIMEOUT and ``roles_left``
+    (int32 [1], optional) the number of waiting warps that left (2)."""
+    _check(status, "status", torch.int32, (1,))
+    if roles_left is not None:
+        _check(roles_left, "roles_left", torch.int32, (1,), status.device)
+    _raise(load().wna16_check_wait_timeout(_ptr(status), _ptr(roles_left), _stream(stream)),
+           "wna16_check_wait_timeout")
 
 
 def read_device_status(status_word: torch.Tensor, stream=None) -> int:
