@@ -219,28 +219,39 @@ def sample_layer(li, tokens, F):
     )
 
 
-def time_oracle(li, target_s, max_tokens=1):
-    """Times oracle.fused_moe_grouped on a sample sized to about ``target_s``
-    seconds; returns (tokens/s, description, seconds)."""
+def size_oracle_sample(li, target_s, max_tokens=1):
+    """The oracle sample (first tokens x first F intermediate features of each
+    routed expert) that takes about ``target_s`` seconds; returns
+    (layer dict, tokens, F, seconds of the last sizing run)."""
     import oracle
 
     wl = li.wl
     unit = 64 if wl.group_size == -1 else max(64, wl.group_size)
     oracle.fused_moe_grouped(sample_layer(li, 1, unit))  # untimed: first-call and thread start-up costs
     F, tokens, dt = unit, 1, 0.0
-    for _ in range(3):  # size the sample from the last timing, up to three rounds
+    for rnd in range(4):  # size the sample from the last timing; the one returned was timed last
         t0 = time.perf_counter()
         oracle.fused_moe_grouped(sample_layer(li, tokens, F))
         dt = max(time.perf_counter() - t0, 1e-4)
-        if dt >= 0.5 * target_s or (F == wl.I and tokens >= max_tokens):
+        if dt >= 0.5 * target_s or (F == wl.I and tokens >= max_tokens) or rnd == 3:
             break
         scale = target_s / dt
         work = tokens * F * scale  # token-features the target allows
         F = int(min(wl.I, max(unit, int(work) // unit * unit)))
         tokens = int(max(1, min(max_tokens, work // wl.I))) if F == wl.I else 1
-    desc = (f"first {tokens} token(s) x first {F} of I={wl.I} intermediate features of each routed expert "
+    return sample_layer(li, tokens, F), tokens, F, dt
+
+
+def oracle_sample_desc(wl, tokens, F):
+    return (f"first {tokens} token(s) x first {F} of I={wl.I} intermediate features of each routed expert "
             f"(work {tokens * F / wl.I:.4f} tokens)")
-    return tokens * F / wl.I / dt, desc, dt
+
+
+def time_oracle(li, target_s, max_tokens=1):
+    """Times oracle.fused_moe_grouped on a sample sized to about ``target_s``
+    seconds; returns (tokens/s, description, seconds)."""
+    _, tokens, F, dt = size_oracle_sample(li, target_s, max_tokens)
+    return tokens * F / li.wl.I / dt, oracle_sample_desc(li.wl, tokens, F), dt
 
 
 def host_cores():
@@ -294,12 +305,19 @@ def reference_arm(args):
     M = args.M
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     li = make_layer_inputs(wl, M, dev, weights=_sample_weights(wl, M, dev, tokens=4))
+    import oracle
+
+    # one sample, sized once to about per_step seconds; every step times it again
     per_step = min(2.0, 150.0 / max(1, args.steps + args.warmup))
-    rates, desc = [], ""
+    L, tokens, F, _ = size_oracle_sample(li, per_step, max_tokens=4)
+    desc = oracle_sample_desc(wl, tokens, F)
+    rates = []
     for i in range(args.warmup + args.steps):
-        r, desc, _ = time_oracle(li, per_step, max_tokens=4)
+        t0 = time.perf_counter()
+        oracle.fused_moe_grouped(L)
+        dt = time.perf_counter() - t0
         if i >= args.warmup:
-            rates.append(r)
+            rates.append(tokens * F / wl.I / dt)
     value = statistics.median(rates)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
