@@ -387,7 +387,13 @@ def _expert_matrices(L, e, cache):
     return cache[e]
 
 
-def fused_moe_per_token(L: dict, tokens=None, round_output=True):
+def _round_intermediate(a: np.ndarray, dtype: str) -> np.ndarray:
+    """The activation rounded once to the activation dtype (nearest-even), as a
+    kernel that stores it in that dtype between the GEMMs would see it."""
+    return halfbits_to_f64(round_to_halfbits(a, dtype), dtype)
+
+
+def fused_moe_per_token(L: dict, tokens=None, round_output=True, round_intermediate=False):
     """The layer, one (token, slot) at a time, in float64.
 
     ``L`` holds: ``x`` [M, H] raw half bits, ``act_dtype``, ``w13_q`` [E, 2I, H/pf],
@@ -402,7 +408,8 @@ def fused_moe_per_token(L: dict, tokens=None, round_output=True):
     g = W13[e, :I] x_t + b13[e, :I], u = W13[e, I:] x_t + b13[e, I:],
     a = act(g, u), y = W2[e] a + b2[e]; out_t = sum_j w[t, j] y_{t,j} in slot
     order. Returns float64 [T, H], or the raw half bits of its single rounding
-    when ``round_output``.
+    when ``round_output``. ``round_intermediate`` (diagnosis only, off for
+    parity) rounds ``a`` to the activation dtype before the down projection.
     """
     x = halfbits_to_f64(L["x"], L["act_dtype"])
     ids = np.asarray(L["topk_ids"])
@@ -426,6 +433,8 @@ def fused_moe_per_token(L: dict, tokens=None, round_output=True):
             if b13 is not None:
                 gu = gu + b13
             a = gated_activation(gu[:I], gu[I:], L.get("glu"))
+            if round_intermediate:
+                a = _round_intermediate(a, L["act_dtype"])
             y = w2 @ a
             b2 = _bias(L, "w2_b", e, L["act_dtype"])
             if b2 is not None:
@@ -436,7 +445,7 @@ def fused_moe_per_token(L: dict, tokens=None, round_output=True):
     return round_to_halfbits(out, L["act_dtype"]) if round_output else out
 
 
-def fused_moe_grouped(L: dict, round_output=True):
+def fused_moe_grouped(L: dict, round_output=True, round_intermediate=False):
     """Same layer, grouped per expert: dequantize one expert at a time and run
     one float64 matrix product over all of its routed (token, slot) pairs.
     Identical mathematics to :func:`fused_moe_per_token`; only the loop order
@@ -459,6 +468,8 @@ def fused_moe_grouped(L: dict, round_output=True):
         if b13 is not None:
             gu = gu + b13[None, :]
         a = gated_activation(gu[:, :I], gu[:, I:], L.get("glu"))
+        if round_intermediate:
+            a = _round_intermediate(a, L["act_dtype"])
         ye = a @ w2.T
         b2 = _bias(L, "w2_b", e, L["act_dtype"])
         if b2 is not None:

@@ -46,3 +46,11 @@ def max_rel_err(y: np.ndarray, r: np.ndarray) -> float:
     if den == 0.0:
         return float(np.max(np.abs(y))) if y.size else 0.0
     return float(np.max(np.abs(y - r)) / den)
+
+
+def norm_rel_err(y: np.ndarray, r: np.ndarray) -> float:
+    """||y - r||_2 / ||r||_2 (reported beside the parity measure)."""
+    y = np.asarray(y, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    den = float(np.linalg.norm(r))
+    return float(np.linalg.norm(y - r)) / den if den else float(np.linalg.norm(y))

@@ -16,7 +16,7 @@ import torch
 import oracle
 import weight_quantized_moe_align_gb300 as w
 from synthetic import WORKLOADS, Workload, make_layer_inputs
-from tests.helpers import bits_to_f64, halfbits, max_rel_err, oracle_layer_dict
+from tests.helpers import bits_to_f64, halfbits, max_rel_err, norm_rel_err, oracle_layer_dict
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -49,7 +49,7 @@ def check(li, block=0, split_k=0, tokens=None):
     r, g = bits_to_f64(ref, dt), bits_to_f64(got, dt)
     assert np.all(np.isfinite(g))
     err = max_rel_err(g, r)
-    assert err <= TOL, (err, block, split_k)
+    assert err <= TOL, (err, norm_rel_err(g, r), block, split_k)
     return err
 
 

@@ -634,3 +634,19 @@ def test_checkpoint_formats_dequantize_like_the_plain_layout(fmt, bits):
     W = (u - z.T[:, g_of_k]) * sf.T[:, g_of_k]
     assert np.array_equal(u, codes) and np.array_equal(z, zeros)
     assert np.array_equal(W, plain)
+
+
+
+def test_round_intermediate_diagnosis_mode():
+    # rounding the activation to the act dtype moves the output by about that
+    # rounding; with codes equal to zero points it changes nothing (a = 0)
+    from tests.helpers import max_rel_err, norm_rel_err
+    L = _small_layer()
+    a = oracle.fused_moe_per_token(L, round_output=False)
+    b = oracle.fused_moe_per_token(L, round_output=False, round_intermediate=True)
+    c = oracle.fused_moe_grouped(L, round_output=False, round_intermediate=True)
+    np.testing.assert_allclose(b, c, rtol=1e-12, atol=1e-15)
+    assert 0 < max_rel_err(b, a) < 2.0 ** -9 and 0 < norm_rel_err(b, a) < 2.0 ** -9
+    Z = dict(L, w13_q=pack_along_last(torch.full((4, 64, 64), 8), 4).numpy(), w13_z=None)
+    assert np.array_equal(oracle.fused_moe_per_token(Z, round_output=False),
+                          oracle.fused_moe_per_token(Z, round_output=False, round_intermediate=True))
