@@ -101,6 +101,8 @@ CONFIGS = [
     (256, 8, "sigmoid", True, 32, 4),    # 32 groups of 8
     (1, 1, "softmax", True, 1, 1),
     (32, 32, "sigmoid", False, 1, 1),    # topk = E
+    (256, 8, "sigmoid", True, 4, 2),     # groups of 64 experts (two 32-wide slots)
+    (64, 6, "softmax", False, 2, 1),     # groups of 32
 ]
 
 
@@ -120,7 +122,7 @@ def test_half_logits(cfg, dt):
     _check(rng.standard_normal((257, E)) * 3.0, k, scoring, renorm, ng, tg, dt=dt)
 
 
-@pytest.mark.parametrize("cfg", CONFIGS[:4] + CONFIGS[9:10])
+@pytest.mark.parametrize("cfg", CONFIGS[:4] + CONFIGS[9:10] + CONFIGS[12:14])
 def test_tied_logits(cfg):
     # integer logits: many exact ties, broken toward the lower index on both sides
     E, k, scoring, renorm, ng, tg = cfg
@@ -141,6 +143,7 @@ def test_non_finite_logits():
         ids, _ = _check(x, 8, scoring, renorm)
         assert all(len(set(r)) == 8 for r in ids.tolist())
     _check(x, 8, "sigmoid", True, n_groups=8, topk_groups=2, max_ambiguous=0.05)
+    _check(x, 8, "sigmoid", True, n_groups=2, topk_groups=1, max_ambiguous=0.05)  # groups of 32
 
 
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
