@@ -424,14 +424,33 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
       float acc[NT];
 #pragma unroll
       for (int j = 0; j < NT; ++j) acc[j] = 0.f;
+      // The previous stage's partial sum is folded in one stage late: its MMA
+      // completion is awaited only once this stage's data has landed.
+      float pscale = 0.f;
+      bool pending = false;
       for (int i = (g - it) & 1; i < n; i += 2) {
         if (!warp_wait_all(&full[cs], cf, abort_flag, a.status)) { ok = false; break; }
+        // the previous stage's MMAs done: A slot, correction rows and P_g free;
+        // its partial sum, scaled into the accumulators
+        if (pending) {
+          if (!warp_wait_all(&pfull[g], pph, abort_flag, a.status)) { ok = false; break; }
+          tc_fence_after();
+          pph ^= 1u;
+#pragma unroll
+          for (int c0 = 0; c0 < NT; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(p_addr + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(pscale, __uint_as_float(v[j]), acc[c0 + j]);
+          }
+        }
         const uint8_t* st = wring + cs * WST;
         const float scale = scale_to_f32<SCL>(reinterpret_cast<const uint16_t*>(st + S_OFF)[si]);
         uint32_t zero = 1u << (BITS - 1);
         if (a.has_zeros) zero = (reinterpret_cast<const uint32_t*>(st + z_off)[zi] >> zshift) & ZMASK;
-        // codes of this row -> A slot g (magic-number form)
         const uint4* src = row_base + cs * (WST / 16);
+        // codes of this row -> A slot g (magic-number form)
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           uint32_t wv[BITS];
@@ -473,22 +492,29 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[g]);
-        // this stage's partial sum, scaled into the accumulators
-        if (!warp_wait_all(&pfull[g], pph, abort_flag, a.status)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < NT; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(p_addr + c0, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(scale, __uint_as_float(v[j]), acc[c0 + j]);
-        }
-        pph ^= 1u;
+        pscale = scale;
+        pending = true;
         cs += 2;
         if (cs >= NS) {
           cs -= NS;
           cf ^= 1u;
+        }
+      }
+      // the unit's last stage
+      if (ok && pending) {
+        if (!warp_wait_all(&pfull[g], pph, abort_flag, a.status)) {
+          ok = false;
+        } else {
+          tc_fence_after();
+          pph ^= 1u;
+#pragma unroll
+          for (int c0 = 0; c0 < NT; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(p_addr + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(pscale, __uint_as_float(v[j]), acc[c0 + j]);
+          }
         }
       }
       it += n;
