@@ -24,8 +24,9 @@
 //   2..5  warpgroup 0: even stages; also the epilogue of every unit
 //   6..9  warpgroup 1: odd stages
 // Warpgroup g owns A slot g and partial-sum buffer P_g: it dequantizes its
-// stage into the slot, builds the stage's correction B rows, signals the MMA
-// warp, waits for the stage's MMAs, and folds P_g into its accumulators. At a
+// stage into the slot, builds the stage's correction B rows and signals the
+// MMA warp; once its next stage's data has landed it waits for those MMAs and
+// folds P_g into its accumulators, then dequantizes that next stage. At a
 // unit's end warpgroup 1 hands its accumulators over in TMEM (buffer C) and
 // warpgroup 0 runs the epilogue; the gate/up epilogue also writes the token
 // sums of its act-cache columns that the down GEMM's correction needs.
