@@ -88,6 +88,29 @@ def algorithmic(wl, M, ids_np):
     )
 
 
+def executed_work(wl, ids_np, block):
+    """What the kernels execute beyond the algorithmic figures: every routed
+    expert's pair count padded up to the GEMM block (the MMA rows run), the
+    flops on those rows, and the bytes of the intermediate buffers (gathered
+    token rows written and read, act cache written and read, fp32 slab written
+    and read), which are implementation traffic, not weight streaming."""
+    ids = ids_np.reshape(-1)
+    cnt = np.bincount(ids[(ids >= 0) & (ids < wl.E)].astype(np.int64), minlength=wl.E)
+    padded = int((-(-cnt // block) * block).sum())
+    P = ids.size
+    return dict(
+        padded_slots=padded,
+        executed_flops=6 * padded * wl.H * wl.I,
+        implementation_bytes=2 * padded * wl.H * 2 + 2 * padded * wl.I * 2 + 2 * P * wl.H * 4,
+    )
+
+
+def step_stats(step_ms):
+    """Median and 10th / 90th percentiles of the per-step times, in us."""
+    t = np.asarray(step_ms, dtype=np.float64) * 1e3
+    return {"median": float(np.median(t)), "p10": float(np.percentile(t, 10)), "p90": float(np.percentile(t, 90))}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -439,6 +462,8 @@ def ours_arm(args):
 
     ids_np = li.topk_ids.cpu().numpy()
     alg = algorithmic(wl, M, ids_np)
+    block = w.choose_block(M, wl.topk, wl.E)
+    exe = executed_work(wl, ids_np, block)
     k1_ms, k2_ms = float(per[:, 2].mean()), float(per[:, 3].mean())
     dom = ("gate_up_gemm", k1_ms, alg["gemm1_bytes"], alg["gemm1_flops"]) if k1_ms >= k2_ms else \
         ("down_gemm", k2_ms, alg["gemm2_bytes"], alg["gemm2_flops"])
@@ -463,14 +488,20 @@ def ours_arm(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.act_dtype, "data": "synthetic",
+        "step_us": step_stats(step_ms),
         "config": {
-            "workload": workload_label(wl, M), "M": M, "block": w.choose_block(M, wl.topk, wl.E),
+            "workload": workload_label(wl, M), "M": M, "block": block,
             "touched_experts": alg["touched"], "l2": "flushed before every step (512 MiB memset, outside the events)",
             "parallelism": f"replicas x{world}",
         },
         "hbm": {"layer_algorithmic_bytes": alg["layer_bytes"], "layer_gbs": alg["layer_bytes"] / layer_s / 1e9,
                 "frac_of_peak": alg["layer_bytes"] / layer_s / 1e9 / peaks["hbm_gbs"],
-                "layer_tflops": alg["layer_flops"] / layer_s / 1e12},
+                "layer_tflops": alg["layer_flops"] / layer_s / 1e12,
+                "roofline_frac": max(alg["layer_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                                     alg["layer_flops"] / (peaks["bf16_tflops"] * 1e12)) / layer_s,
+                "padded_slots": exe["padded_slots"], "routed_pairs": M * wl.topk,
+                "executed_tflops": exe["executed_flops"] / layer_s / 1e12,
+                "implementation_bytes": exe["implementation_bytes"]},
         "kernels_ms": {"align": float(per[:, 0].mean()), "gather": float(per[:, 1].mean()),
                        "gate_up_gemm": k1_ms, "down_gemm": k2_ms, "combine": float(per[:, 4].mean())},
         "roofline": roof,
@@ -489,12 +520,17 @@ def ours_arm(args):
             lix, _, _, callx = setup(Mx)
             perx = timed(callx, args.sweep_steps, 3)
             s = float(whole_steps(callx, args.sweep_steps, 3)[0].mean()) / 1e3
-            a = algorithmic(wl, Mx, lix.topk_ids.cpu().numpy())
+            idsx = lix.topk_ids.cpu().numpy()
+            a = algorithmic(wl, Mx, idsx)
+            bx = w.choose_block(Mx, wl.topk, wl.E)
+            ex = executed_work(wl, idsx, bx)
+            hf = a["layer_bytes"] / s / 1e9 / peaks["hbm_gbs"]
+            tf = a["layer_flops"] / s / 1e12 / peaks["bf16_tflops"]
             sweep.append({"M": Mx, "us": s * 1e6, "tokens_per_s": Mx / s, "hbm_gbs": a["layer_bytes"] / s / 1e9,
-                          "hbm_frac": a["layer_bytes"] / s / 1e9 / peaks["hbm_gbs"],
-                          "tflops": a["layer_flops"] / s / 1e12,
-                          "tensor_frac": a["layer_flops"] / s / 1e12 / peaks["bf16_tflops"],
-                          "touched_experts": a["touched"], "block": w.choose_block(Mx, wl.topk, wl.E),
+                          "hbm_frac": hf, "tflops": a["layer_flops"] / s / 1e12, "tensor_frac": tf,
+                          "roofline_frac": max(hf, tf), "padded_slots": ex["padded_slots"],
+                          "executed_tflops": ex["executed_flops"] / s / 1e12,
+                          "touched_experts": a["touched"], "block": bx,
                           "kernels_us": [float(v) * 1e3 for v in perx.mean(axis=0)]})
             del lix, callx
         line["sweep"] = sweep
