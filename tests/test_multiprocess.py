@@ -37,7 +37,7 @@ def _rank_main(rank, world, port, results):
 
 def test_job_time_is_the_slowest_rank_and_value_counts_all_ranks():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), results), nprocs=world, join=True)
         res = dict(results)
