@@ -113,8 +113,16 @@ wna16_status wna16_moe_align_block_size(const int32_t* topk_ids, int64_t M, int 
                                         int32_t* device_status, void* stream);
 
 /*
- * Block size the fused call uses when given block = 0: the power of two in
- * [16, 256] closest to the expected pairs per active expert.
+ * Block size the fused call uses when given block = 0, from the average routed
+ * pairs per active expert, avg = M * topk / min(M * topk, E) (the routing
+ * itself is not seen on the host):
+ *   avg <= 64 (weight streaming dominates): the tile of 16, 32 or 64 tokens
+ *     with the least estimated streaming cost, ceil(1.3 * avg / tile) passes
+ *     over the expert's weights times the measured cost of one pass with that
+ *     tile (1.0, 1.28, 1.34);
+ *   avg > 64 (tensor-bound): the smallest power of two >= avg, from 64 up to
+ *     128.
+ * Returns 16 when M * topk <= 0.
  */
 int wna16_choose_block(int64_t M, int topk, int E);
 
