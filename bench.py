@@ -319,6 +319,16 @@ def aggregate_ranks(total_ms, M, steps, dist=None, device="cpu"):
     return total_ms, world * M * steps / (total_ms / 1000.0)
 
 
+L2_POLICY = ("GPU arm: L2 flushed before every step (512 MiB memset, outside the timed events); "
+             "CPU oracle arm: host caches not flushed")
+
+
+def run_config(wl, M, world):
+    """The ``config`` object of both arms' JSON lines: the workload and batch,
+    how caches are treated between steps, and the replica count."""
+    return {"workload": workload_label(wl, M), "M": M, "l2": L2_POLICY, "parallelism": f"replicas x{world}"}
+
+
 def reference_arm(args):
     """The oracle as it stands, on the host cores, on a bounded sample per step."""
     rank = int(os.environ.get("RANK", "0"))
@@ -334,20 +344,25 @@ def reference_arm(args):
     per_step = min(2.0, 150.0 / max(1, args.steps + args.warmup))
     L, tokens, F, _ = size_oracle_sample(li, per_step, max_tokens=4)
     desc = oracle_sample_desc(wl, tokens, F)
-    rates = []
+    work = tokens * F / wl.I  # tokens of the workload one step computes
+    secs = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         oracle.fused_moe_grouped(L)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
-            rates.append(tokens * F / wl.I / dt)
-    value = statistics.median(rates)
+            secs.append(dt)
+    # every timed step ran the same sample: value = its work over the total time
+    total_s = float(sum(secs))
+    value = work * len(secs) / total_s
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * M / value,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total_s / len(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": workload_label(wl, M), "M": M},
+        "config": run_config(wl, M, 1),
+        "work_tokens_per_step": work,
+        "step_s": {"median": statistics.median(secs), "min": min(secs), "max": max(secs)},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -489,11 +504,8 @@ def ours_arm(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.act_dtype, "data": "synthetic",
         "step_us": step_stats(step_ms),
-        "config": {
-            "workload": workload_label(wl, M), "M": M, "block": block,
-            "touched_experts": alg["touched"], "l2": "flushed before every step (512 MiB memset, outside the events)",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": run_config(wl, M, world),
+        "launch_config": {"block": block, "touched_experts": alg["touched"]},
         "hbm": {"layer_algorithmic_bytes": alg["layer_bytes"], "layer_gbs": alg["layer_bytes"] / layer_s / 1e9,
                 "frac_of_peak": alg["layer_bytes"] / layer_s / 1e9 / peaks["hbm_gbs"],
                 "layer_tflops": alg["layer_flops"] / layer_s / 1e12,
