@@ -242,13 +242,14 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
  *     batches of the supported layers fit; large prefill batches do not: use
  *     wna16_fused_moe with a workspace for those).
  *   - The first call on a device looks up the area's device address on the
- *     current device (a one-time set-up per device); make that first call
- *     before any stream capture.
+ *     current device (a one-time set-up per device, repeated only if the
+ *     device's CUDA context was replaced, e.g. after cudaDeviceReset); make
+ *     that first call before any stream capture.
  *   - Every call on a device shares the one area, which keeps whatever the
  *     last call left in it. Each call rewrites everything it later reads (the
  *     device status word at its start is reset by the call), so nothing has
- *     to be cleared between calls; that status word is not reachable from
- *     outside the library.
+ *     to be cleared between calls. wna16_noalloc_read_status reads that
+ *     status word (the errors found on the device by the last call).
  *   - Calls whose GPU execution overlaps (issued on different streams, or
  *     from different host threads without ordering) race on the area and
  *     corrupt each other's results: serialize them.
@@ -261,6 +262,16 @@ wna16_status wna16_fused_moe_noalloc(const void* hidden, wna16_dtype act_dtype, 
                                      int group_size, const int32_t* topk_ids,
                                      const float* topk_weights, void* out, int block, int split_k,
                                      void* stream);
+
+/*
+ * The device status word of the last wna16_fused_moe_noalloc call on the
+ * current device (the pages have no counterpart either): the
+ * wna16_read_device_status of the library-owned area. Synchronizes `stream`
+ * (issue it on the stream of that call, or after it completed), writes the
+ * raw WNA16_DEV_* bits to *bits_out (may be NULL) and returns as
+ * wna16_read_device_status does.
+ */
+wna16_status wna16_noalloc_read_status(int32_t* bits_out, void* stream);
 
 /*
  * Prepacked weights (optional, a one-time conversion at load time).

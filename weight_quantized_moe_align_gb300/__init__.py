@@ -19,6 +19,7 @@ from .binding import (  # noqa: F401
     fused_moe_routed,
     load,
     moe_align_block_size,
+    noalloc_read_status,
     prepack,
     read_device_status,
     topk_routing,

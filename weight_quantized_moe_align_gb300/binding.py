@@ -34,7 +34,7 @@ EXPORTED = (
     "wna16_fused_moe_noalloc", "wna16_prepack_bytes", "wna16_prepack", "wna16_fused_moe_prepacked",
     "wna16_read_device_status", "wna16_status_string", "wna16_topk_routing", "wna16_fused_moe_ex",
     "wna16_fused_moe_prepacked_ex", "wna16_act_order_prepare", "wna16_convert_checkpoint",
-    "wna16_check_wait_timeout",
+    "wna16_check_wait_timeout", "wna16_noalloc_read_status",
 )
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
@@ -113,6 +113,8 @@ def load() -> ctypes.CDLL:
     L.wna16_fused_moe_timed.restype = i32
     L.wna16_fused_moe_noalloc.argtypes = L.wna16_fused_moe.argtypes[:19] + [i32, i32, vp]
     L.wna16_fused_moe_noalloc.restype = i32
+    L.wna16_noalloc_read_status.argtypes = [c.POINTER(c.c_int32), vp]
+    L.wna16_noalloc_read_status.restype = i32
     L.wna16_prepack_bytes.argtypes = [i32, i64, i64, i32, i32, i32, i32]
     L.wna16_prepack_bytes.restype = sz
     L.wna16_prepack.argtypes = [vp, vp, vp, i32, i64, i64, i32, i32, i32, vp, vp]
@@ -400,6 +402,16 @@ def fused_moe_noalloc(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: tor
         group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out), block, split_k, _stream(stream))
     _raise(st, "wna16_fused_moe_noalloc")
     return out
+
+
+def noalloc_read_status(stream=None) -> int:
+    """Synchronizes the stream and returns the raw device status bits of the
+    last ``fused_moe_noalloc`` call on the current device."""
+    bits = ctypes.c_int32(0)
+    st = load().wna16_noalloc_read_status(ctypes.byref(bits), _stream(stream))
+    if st not in (0, 5, 6, 7):
+        _raise(st, "wna16_noalloc_read_status")
+    return int(bits.value)
 
 
 class PackedWeights:
