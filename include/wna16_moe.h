@@ -183,6 +183,12 @@ size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, i
  *                its first int32 is the device status word (reset by the call).
  *   block        align block size (0 = automatic), as in
  *                wna16_moe_align_block_size; it is also the GEMM token tile.
+ *                Forced sizes other than the automatic choice are verified on
+ *                the GPU for layers of up to 64 experts. With more experts they
+ *                are accepted but unverified: one run of forced 32/64/128 on a
+ *                256-expert layer at M = 256 ended in an unexplained launch
+ *                failure, although wna16_check_launch_plan finds every index
+ *                of those launch plans in bounds.
  *   split_k      K-splits of the down GEMM (0 = automatic, else 1..8).
  * Shapes: H a multiple of 64, I a multiple of 64, 1 <= topk <= E <= 256,
  * M*topk < 2^31. M = 0 returns WNA16_OK and launches nothing.
@@ -454,6 +460,30 @@ wna16_status wna16_read_device_status(const void* status_word, int32_t* bits_out
  * freed and the context stays usable. Asynchronous on `stream`.
  */
 wna16_status wna16_check_wait_timeout(int32_t* device_status, int32_t* roles_left, void* stream);
+
+/*
+ * Host-only check of one fused call's launch plan (no GPU, no CUDA call):
+ * builds the plan wna16_fused_moe would launch for these sizes on a device
+ * with `sms` SMs (plain weight layout, default options), and replays every
+ * role of every CTA of both GEMM launches, plus the gather and the combine,
+ * through the kernels' own index expressions, on the given align output
+ * (host arrays: topk_ids [M, topk], sorted_ids [cap], expert_ids [cap/block]
+ * and num_tokens_post_padded, e.g. from a reference implementation of
+ * moe_align_block_size with the same block). It checks that every TMA box lies
+ * inside its tensor map with a 16-byte-aligned innermost coordinate, that a
+ * stage's boxes add up to the bytes its barrier expects, that the work units
+ * cover every (block, weight tile, K split) once, that tensor-memory and
+ * shared-memory layouts fit and do not overlap, and that every global write
+ * lands inside its workspace region, each routed pair's fp32 rows written once.
+ * Returns the number of violations (0: all in bounds), or minus a
+ * wna16_status for arguments the fused call would reject. The first few
+ * violations are written, one per line, to `report` (may be NULL).
+ */
+int64_t wna16_check_launch_plan(int64_t M, int64_t H, int64_t I, int E, int topk, int bits, int group_size,
+                                int has_zeros, wna16_dtype act_dtype, wna16_dtype scale_dtype, int block,
+                                int split_k, int sms, const int32_t* topk_ids, const int32_t* sorted_ids,
+                                const int32_t* expert_ids, int32_t num_tokens_post_padded, char* report,
+                                size_t report_bytes);
 
 /* Static, human-readable name of a status code. */
 const char* wna16_status_string(wna16_status status);

@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     act_order_prepare,
     WNA16Error,
     align_capacity,
+    check_launch_plan,
     check_wait_timeout,
     choose_block,
     convert_checkpoint,

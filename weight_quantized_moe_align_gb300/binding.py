@@ -34,7 +34,7 @@ EXPORTED = (
     "wna16_fused_moe_noalloc", "wna16_prepack_bytes", "wna16_prepack", "wna16_fused_moe_prepacked",
     "wna16_read_device_status", "wna16_status_string", "wna16_topk_routing", "wna16_fused_moe_ex",
     "wna16_fused_moe_prepacked_ex", "wna16_act_order_prepare", "wna16_convert_checkpoint",
-    "wna16_check_wait_timeout", "wna16_noalloc_read_status",
+    "wna16_check_wait_timeout", "wna16_noalloc_read_status", "wna16_check_launch_plan",
 )
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
@@ -136,6 +136,9 @@ def load() -> ctypes.CDLL:
     L.wna16_act_order_prepare.restype = i32
     L.wna16_topk_routing.argtypes = [vp, i32, i64, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     L.wna16_topk_routing.restype = i32
+    L.wna16_check_launch_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp,
+                                          vp, c.c_int32, c.c_char_p, sz]
+    L.wna16_check_launch_plan.restype = i64
     L.wna16_status_string.argtypes = [i32]
     L.wna16_status_string.restype = c.c_char_p
     _lib = L
@@ -557,6 +560,24 @@ def check_wait_timeout(status: torch.Tensor, roles_left: Optional[torch.Tensor] 
         _check(roles_left, "roles_left", torch.int32, (1,), status.device)
     _raise(load().wna16_check_wait_timeout(_ptr(status), _ptr(roles_left), _stream(stream)),
            "wna16_check_wait_timeout")
+
+
+def check_launch_plan(M, H, I, E, topk, bits, group_size, has_zeros, act_dtype, scale_dtype, topk_ids, sorted_ids,
+                      expert_ids, num_tokens_post_padded, block=0, split_k=0, sms=152):
+    """Host-only replay of a fused call's launch plan on a given align output
+    (``wna16_check_launch_plan``; numpy int32 arrays). Returns (violations,
+    report text)."""
+    import numpy as np
+
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    srt = np.ascontiguousarray(sorted_ids, dtype=np.int32)
+    exp = np.ascontiguousarray(expert_ids, dtype=np.int32)
+    buf = ctypes.create_string_buffer(4096)
+    dt = {"f16": 0, "bf16": 1}
+    n = load().wna16_check_launch_plan(M, H, I, E, topk, bits, group_size, int(bool(has_zeros)), dt[act_dtype],
+                                       dt[scale_dtype], block, split_k, sms, ids.ctypes.data, srt.ctypes.data,
+                                       exp.ctypes.data, int(num_tokens_post_padded), buf, len(buf))
+    return int(n), buf.value.decode()
 
 
 def read_device_status(status_word: torch.Tensor, stream=None) -> int:

@@ -43,16 +43,11 @@
 namespace wna16 {
 
 constexpr int kDeferThreads = 10 * 32;
-// TMEM columns: P_0 [0,16), P_1 [16,32), C [32,48); A slot g at 64 + 96 g:
+// TMEM columns (plan.cuh): P_0 [0,16), P_1 [16,32), C [32,48); A slot g at 64 + 96 g:
 // 64 columns for the 128 K of the stage, then 8 columns for the correction.
 // Combine buffer C: its own 16 columns at [32, 48) for 16-token tiles; for
 // 32-token tiles it is P_1 itself (the TMEM budget has no room for a third
 // 32-column buffer), which warpgroup 1 may reuse only after warpgroup 0 took C.
-template <int NT>
-__host__ __device__ constexpr int defer_c_col() { return NT == 16 ? 32 : NT; }
-constexpr int kDeferA0 = 64;
-constexpr int kDeferAStride = 96;
-constexpr int kDeferTmemCols = 256;
 
 // Codes of 32 consecutive K elements (one 16-column TMEM chunk) in magic-number
 // form, same pair order as Dequant (int4: pairs (k_j, k_j+4) of every word).
@@ -199,19 +194,20 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
   const int lane = threadIdx.x & 31;
   const int NS = a.num_stages;
 
-  uint8_t* wring = smem;
-  uint8_t* bring = smem + weight_ring_bytes(BITS, NS);
-  uint8_t* bcorr = bring + NS * BST;                              // 2 tiles of NT rows x 128 B
-  float* xring = reinterpret_cast<float*>(bcorr + 2 * NT * 128);  // NS x [XPARTS][NT]
-  uint64_t* full = reinterpret_cast<uint64_t*>(xring + NS * (XST / 4));
+  const SmemLayout sl = defer_smem_layout(BITS, GEMM, NT, NS);
+  uint8_t* wring = smem + sl.wring;
+  uint8_t* bring = smem + sl.bring;
+  uint8_t* bcorr = smem + sl.bcorr;                          // 2 tiles of NT rows x 128 B
+  float* xring = reinterpret_cast<float*>(smem + sl.xring);  // NS x [XPARTS][NT]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + sl.bars);
   uint64_t* empty = full + NS;
   uint64_t* afull = empty + NS;  // [2]
   uint64_t* pfull = afull + 2;   // [2]
   uint64_t* cfull = pfull + 2;
   uint64_t* cempty = cfull + 1;
   uint64_t* drain = cempty + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + sl.holder);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + sl.abort_flag);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -249,14 +245,12 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
   // (block count, expert of each block) were complete before the previous
   // kernel started: read from L2 without waiting. Everything the previous
   // kernel writes is read after grid_dep_wait().
-  int nb = __ldcg(a.num_post_pad) / NT;
-  nb = nb < 0 ? 0 : (nb > a.max_blocks ? a.max_blocks : nb);
+  const int nb = active_blocks(__ldcg(a.num_post_pad), NT, a.max_blocks);
   const int units = nb * a.n_tiles * a.split;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    const uint32_t stage_tx =
-        ((VAR && a.wpack) ? a.wimg : W_BYTES + 256 + (a.has_zeros ? (kTileRows / PF) * 4 : 0)) + BST + XST;
+    const uint32_t stage_tx = weight_stage_tx(BITS, 1, a.has_zeros, (VAR && a.wpack) ? a.wimg : 0) + BST + XST;
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_b = l2_policy_evict_last();
     int it = 0, s = 0;
@@ -270,25 +264,25 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
       uint8_t* dst = wring + s * WST;
       if (VAR && a.wpack) {
         // prepacked: the stage's codes, scales and zero points as one image
-        const uint8_t* src = a.wpack + ((static_cast<size_t>(e) * a.n_tiles + w.tile) * a.kt_total + kt) * a.wimg;
-        bulk_load(dst, src, a.wimg, &full[s], pol_w);
-      } else if (GEMM == 1) {
-        const int f0 = w.tile * kGateUpRows;
-        tma_load_3d(dst, &tm_q, &full[s], kt * KW, f0, 2 * e, pol_w);
-        tma_load_3d(dst + S_OFF, &tm_s, &full[s], f0, 0, ys, pol_w);
-        if (a.has_zeros) tma_load_3d(dst + Z_OFF, &tm_z, &full[s], f0 / PF, 0, ys, pol_w);
+        bulk_load(dst, a.wpack + image_offset(a, e, w.tile, kt), a.wimg, &full[s], pol_w);
+        return;
+      }
+      const StageCoords c = weight_stage_coords(GEMM, BITS, a, w.tile, e, kt, ys);
+      if (GEMM == 1) {
+        tma_load_3d(dst, &tm_q, &full[s], c.q[0], c.q[1], c.q[2], pol_w);
+        tma_load_3d(dst + S_OFF, &tm_s, &full[s], c.s[0], c.s[1], c.s[2], pol_w);
+        if (a.has_zeros) tma_load_3d(dst + Z_OFF, &tm_z, &full[s], c.z[0], c.z[1], c.z[2], pol_w);
       } else {
-        const int r0 = w.tile * kTileRows;
-        tma_load_2d(dst, &tm_q, &full[s], kt * KW, e * a.N + r0, pol_w);
-        tma_load_2d(dst + S_OFF, &tm_s, &full[s], r0, ys, pol_w);
-        if (a.has_zeros) tma_load_2d(dst + Z_OFF, &tm_z, &full[s], r0 / PF, ys, pol_w);
+        tma_load_2d(dst, &tm_q, &full[s], c.q[0], c.q[1], pol_w);
+        tma_load_2d(dst + S_OFF, &tm_s, &full[s], c.s[0], c.s[1], pol_w);
+        if (a.has_zeros) tma_load_2d(dst + Z_OFF, &tm_z, &full[s], c.z[0], c.z[1], pol_w);
       }
     };
     auto load_tokens = [&](int s, const Unit& w, int kt) {
 #pragma unroll
       for (int c = 0; c < kTileK / kChunkK; ++c)
-        tma_load_2d(bring + s * BST + c * NT * 128, &tm_b, &full[s], kt * kTileK + c * kChunkK, w.blk * NT, pol_b);
-      tma_load_3d(xring + s * (XST / 4), &tm_x, &full[s], w.blk * NT, 0, kt, pol_b);
+        tma_load_2d(bring + s * BST + c * NT * 128, &tm_b, &full[s], token_x(kt, c), token_y(w.blk, NT), pol_b);
+      tma_load_3d(xring + s * (XST / 4), &tm_x, &full[s], token_y(w.blk, NT), 0, kt, pol_b);
     };
     // The first ring's worth of weight stages is requested before waiting for
     // the previous kernel (its slots are fresh); their token parts follow the
@@ -358,8 +352,8 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         if (!warp_wait_all(&afull[g], (it >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
         if (elect_one()) {
-          const uint32_t d = tmem + g * NT;
-          const uint32_t at = tmem + kDeferA0 + g * kDeferAStride;
+          const uint32_t d = tmem + defer_p_col(g, NT);
+          const uint32_t at = tmem + defer_a_col(g);
           const uint64_t b0 = smem_desc_sw128(smem_u32(bring + s * BST));
           const uint64_t b1 = b0 + chunk_step;
           mma_ts_first(d, at, b0, idesc);
@@ -405,9 +399,9 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     const int zshift = BITS * (hrow % PF);
     const int z_off = (VAR && a.wpack) ? W_BYTES + 256 : Z_OFF;  // zero points: right after the scales in an image
     const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t a_slot = tmem + t_lane + kDeferA0 + g * kDeferAStride;
-    const uint32_t p_addr = tmem + t_lane + g * NT;
-    const uint32_t c_addr = tmem + t_lane + defer_c_col<NT>();
+    const uint32_t a_slot = tmem + t_lane + defer_a_col(g);
+    const uint32_t p_addr = tmem + t_lane + defer_p_col(g, NT);
+    const uint32_t c_addr = tmem + t_lane + defer_c_col(NT);
     const bool builder = ((warp - 2) & 3) == 0 && lane < NT;  // first warp of the group writes the B rows
     uint8_t* my_bcorr = bcorr + g * NT * 128;
     const uint4* row_base = reinterpret_cast<const uint4*>(wring + srow * KW * 4);
@@ -536,7 +530,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(cfull);
         // C aliases P_1: the next MMA into it must wait until warpgroup 0 took C
-        if (defer_c_col<NT>() == NT && !warp_wait_all(cempty, uc & 1, abort_flag, a.status)) break;
+        if (defer_c_col(NT) == NT && !warp_wait_all(cempty, uc & 1, abort_flag, a.status)) break;
         continue;
       }
       if (!warp_wait_all(cfull, uc & 1, abort_flag, a.status)) break;
@@ -556,14 +550,13 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         // K split: each split unit publishes its fp32 partial sums; per lane
         // quarter, the last of the split units to arrive adds them up in split
         // order (deterministic) and runs the epilogue. The others stop here.
-        const size_t unit_base = (static_cast<size_t>(w.tile) * a.max_blocks + w.blk) * a.split;
         const int row = q * 32 + lane;  // TMEM lane = row of the 128-row tile
-        float4* mine = reinterpret_cast<float4*>(a.part + ((unit_base + w.sp) * kTileRows + row) * NT);
+        float4* mine = reinterpret_cast<float4*>(a.part + part_index(a, w.tile, w.blk, w.sp, row, NT));
 #pragma unroll
         for (int j = 0; j < NT; j += 4) mine[j / 4] = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
         __threadfence();
         __syncwarp();
-        int* counter = a.counters + (static_cast<size_t>(w.tile) * a.max_blocks + w.blk) * 4 + q;
+        int* counter = a.counters + counter_index(a, w.tile, w.blk, q);
         int arrived = 0;
         if (lane == 0) arrived = atomicAdd(counter, 1);
         arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
@@ -572,7 +565,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
 #pragma unroll
         for (int j = 0; j < NT; ++j) acc[j] = 0.f;
         for (int sp = 0; sp < a.split; ++sp) {
-          const float4* src = reinterpret_cast<const float4*>(a.part + ((unit_base + sp) * kTileRows + row) * NT);
+          const float4* src = reinterpret_cast<const float4*>(a.part + part_index(a, w.tile, w.blk, sp, row, NT));
 #pragma unroll
           for (int j = 0; j < NT; j += 4) {
             const float4 v4 = __ldcg(src + j / 4);
@@ -606,14 +599,15 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
           const float val = VAR ? gate_up_act(a, gt, up) : gt / (1.0f + __expf(-gt)) * up;
           const int col = lo ? j : j + NT / 2;
           const size_t row = static_cast<size_t>(w.blk) * NT + col;
+          const size_t idx = act_index(w.blk, NT, col, a.I, fp);
           float stored;
           if constexpr (ACT == 0) {
             const __half hv = __float2half_rn(val);
-            act[row * a.I + fp] = hv;
+            act[idx] = hv;
             stored = __half2float(hv);
           } else {
             const __nv_bfloat16 hv = __float2bfloat16_rn(val);
-            act[row * a.I + fp] = hv;
+            act[idx] = hv;
             stored = __bfloat162float(hv);
           }
           // token sums of the stored values over this warp's 16 features, by
@@ -624,7 +618,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
           stored += __shfl_xor_sync(0xFFFFFFFFu, stored, 8);
           if ((lane & 14) == 0) {
             const int part = (w.tile & 1) * 8 + q * 2 + (lane & 1);
-            a.xs_out[(static_cast<size_t>(w.tile >> 1) * 16 + part) * a.cap + row] = stored;
+            a.xs_out[xs_out_index(w.tile, part, a.cap, row)] = stored;
           }
         }
       } else {
@@ -643,7 +637,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
           const int pid = __shfl_sync(0xFFFFFFFFu, my_pid, j);
           const float tw = __shfl_sync(0xFFFFFFFFu, my_w, j);
           if (pid >= 0 && pid < a.P && hr < a.N)
-            slab[(static_cast<size_t>(w.sp) * a.P + pid) * a.N + hr] = acc[j] * tw;
+            slab[slab_index(w.sp, a.P, pid, a.N, hr)] = acc[j] * tw;
         }
       }
     }

@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "plan.cuh"
 #include "ptx.cuh"
 
 namespace wna16 {
@@ -174,42 +175,14 @@ struct Dequant {
   }
 };
 
-struct Unit {
-  int blk, tile, sp, kt0, kt1;
-};
-
-// Work-unit order (the same in every role): panels of a.panel consecutive
-// token blocks (the align output is expert-sorted, so a panel spans one or a
-// few experts); inside a panel the weight tile is the slowest index and the K
-// split the fastest. Concurrent CTAs then share a panel's token rows and each
-// weight tile across the panel's blocks. The host sizes panels so that their
-// token rows stay well inside L2; small batches get one panel.
-__device__ __forceinline__ Unit decode_unit(int u, int nb, const GemmArgs& a) {
-  Unit r;
-  const int panel_units = a.panel * a.n_tiles * a.split;
-  const int p = u / panel_units;
-  const int b0 = p * a.panel;
-  const int pbs = nb - b0 < a.panel ? nb - b0 : a.panel;  // blocks in this panel
-  int rest = u - p * panel_units;
-  r.sp = rest % a.split;
-  rest /= a.split;
-  r.blk = b0 + rest % pbs;
-  r.tile = rest / pbs;
-  r.kt0 = static_cast<int>(static_cast<long long>(a.kt_total) * r.sp / a.split);
-  r.kt1 = static_cast<int>(static_cast<long long>(a.kt_total) * (r.sp + 1) / a.split);
-  return r;
-}
-
 __device__ __forceinline__ int unit_expert(const GemmArgs& a, int blk) {
-  const int e = a.expert_ids[blk];
-  return (e >= 0 && e < a.E) ? e : 0;  // blocks below num_post_pad always hold a valid id
+  return clamp_expert(a.expert_ids[blk], a.E);  // blocks below num_post_pad always hold a valid id
 }
 
 // The same read from L2 (the align kernel's output, read by a kernel that may
 // have started before its predecessor finished).
 __device__ __forceinline__ int unit_expert_l2(const GemmArgs& a, int blk) {
-  const int e = __ldcg(a.expert_ids + blk);
-  return (e >= 0 && e < a.E) ? e : 0;
+  return clamp_expert(__ldcg(a.expert_ids + blk), a.E);
 }
 
 // Epilogue of one work unit, run by four warps covering the four TMEM lane
@@ -224,7 +197,7 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
   const int NT = a.block;
   if (!warp_wait_all(&accfull[acc], acc_phase, abort_flag, a.status)) return false;
   tc_fence_after();
-  const uint32_t t_base = tmem + ((q * 32) << 16) + acc * NT;
+  const uint32_t t_base = tmem + ((q * 32) << 16) + gemm_acc_col(acc, NT);
   // bias of this lane's row: gate/up GEMM, gate row f (lanes 0-15) or up row
   // I + f (16-31); down GEMM, row h, added by the first K split only
   float bias = 0.f;
@@ -277,12 +250,12 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
         const float up = __uint_as_float(lo ? other : mine);
         const float val = EXT ? gate_up_act(a, g, up) : g / (1.0f + __expf(-g)) * up;
         const int col = c0 + (lo ? j : j + 8);
-        const size_t row = static_cast<size_t>(w.blk) * NT + col;
         if (!fp_ok) continue;
+        const size_t idx = act_index(w.blk, NT, col, a.I, fp);
         if constexpr (ACT == 0)
-          act[row * a.I + fp] = __float2half_rn(val);
+          act[idx] = __float2half_rn(val);
         else
-          act[row * a.I + fp] = __float2bfloat16_rn(val);
+          act[idx] = __float2bfloat16_rn(val);
       }
     } else {
       float* slab = reinterpret_cast<float*>(a.out);
@@ -294,7 +267,7 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
         const int pid = __shfl_sync(0xFFFFFFFFu, my_pid, j);
         const float tw = __shfl_sync(0xFFFFFFFFu, my_w, j);
         if (pid >= 0 && pid < a.P && h < a.N)
-          slab[(static_cast<size_t>(w.sp) * a.P + pid) * a.N + h] = __uint_as_float(v[j]) * tw;
+          slab[slab_index(w.sp, a.P, pid, a.N, h)] = __uint_as_float(v[j]) * tw;
       }
     }
   }
@@ -334,17 +307,17 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
   const int BST = token_stage_bytes(NT);
   const int SG = a.G < kTileK ? kTileK / a.G : 1;  // group rows per stage (G = 64 -> 2)
 
-  uint8_t* wring = smem;
-  uint8_t* bring = smem + weight_ring_bytes(BITS, NS);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(bring + NS * BST);
-  uint64_t* full = bars;             // stage landed: codes, scales, zeros and token tile
+  const SmemLayout sl = gemm_smem_layout(BITS, NT, NS, NA, NACC);
+  uint8_t* wring = smem + sl.wring;
+  uint8_t* bring = smem + sl.bring;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + sl.bars);  // stage landed: codes, scales, zeros, token tile
   uint64_t* empty = full + NS;       // stage consumed: its MMAs completed (also frees its A slot)
   uint64_t* afull = empty + NS;      // A slot written by a dequant warpgroup
   uint64_t* accfull = afull + NA;    // accumulator ready for the epilogue
   uint64_t* accempty = accfull + NACC;
   uint64_t* drain = accempty + NACC;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + sl.holder);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + sl.abort_flag);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -380,8 +353,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
   grid_dep_wait();
   grid_dep_launch();
 
-  int nb = *a.num_post_pad / NT;
-  nb = nb < 0 ? 0 : (nb > a.max_blocks ? a.max_blocks : nb);
+  const int nb = active_blocks(*a.num_post_pad, NT, a.max_blocks);
   const int units = nb * a.n_tiles * a.split;
 
   if (warp == 0) {
@@ -391,8 +363,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     // 64-wide K chunks of the token tile: five copies for 8-16 KB of codes.
     // The whole warp runs the loop (waits are warp-wide polls); one elected
     // lane issues the copies.
-    const uint32_t stage_tx =
-        ((EXT && a.wpack) ? a.wimg : W_BYTES + SG * 256 + (a.has_zeros ? SG * (kTileRows / PF) * 4 : 0)) + BST;
+    const uint32_t stage_tx = weight_stage_tx(BITS, SG, a.has_zeros, (EXT && a.wpack) ? a.wimg : 0) + BST;
     const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
     const uint64_t pol_b = l2_policy_evict_last();   // token rows: re-read by every row tile
     int it = 0, s = 0;
@@ -406,28 +377,26 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
         if (elect_one()) {
           mbar_arrive_expect_tx(&full[s], stage_tx);
           uint8_t* dst = wring + s * WST;
-          const int ys = e * a.groups + (kt * kTileK) / a.G;
+          const int ys = stage_group_row(a, e, kt);
           if (EXT && a.wpack) {
             // prepacked: the stage's codes, scales and zero points as one image
-            const uint8_t* src =
-                a.wpack + ((static_cast<size_t>(e) * a.n_tiles + w.tile) * a.kt_total + kt) * a.wimg;
-            bulk_load(dst, src, a.wimg, &full[s], pol_w);
-          } else if (GEMM == 1) {
-            const int f0 = w.tile * kGateUpRows;
-            tma_load_3d(dst, &tm_q, &full[s], kt * KW, f0, 2 * e, pol_w);
-            tma_load_3d(dst + S_OFF, &tm_s, &full[s], f0, 0, ys, pol_w);
-            if (a.has_zeros) tma_load_3d(dst + Z_OFF, &tm_z, &full[s], f0 / PF, 0, ys, pol_w);
+            bulk_load(dst, a.wpack + image_offset(a, e, w.tile, kt), a.wimg, &full[s], pol_w);
           } else {
-            const int r0 = w.tile * kTileRows;
-            tma_load_2d(dst, &tm_q, &full[s], kt * KW, e * a.N + r0, pol_w);
-            tma_load_2d(dst + S_OFF, &tm_s, &full[s], r0, ys, pol_w);
-            if (a.has_zeros) tma_load_2d(dst + Z_OFF, &tm_z, &full[s], r0 / PF, ys, pol_w);
+            const StageCoords c = weight_stage_coords(GEMM, BITS, a, w.tile, e, kt, ys);
+            if (GEMM == 1) {
+              tma_load_3d(dst, &tm_q, &full[s], c.q[0], c.q[1], c.q[2], pol_w);
+              tma_load_3d(dst + S_OFF, &tm_s, &full[s], c.s[0], c.s[1], c.s[2], pol_w);
+              if (a.has_zeros) tma_load_3d(dst + Z_OFF, &tm_z, &full[s], c.z[0], c.z[1], c.z[2], pol_w);
+            } else {
+              tma_load_2d(dst, &tm_q, &full[s], c.q[0], c.q[1], pol_w);
+              tma_load_2d(dst + S_OFF, &tm_s, &full[s], c.s[0], c.s[1], pol_w);
+              if (a.has_zeros) tma_load_2d(dst + Z_OFF, &tm_z, &full[s], c.z[0], c.z[1], pol_w);
+            }
           }
           // token tile: the block's rows of the expert-sorted token matrix
 #pragma unroll
           for (int c = 0; c < kTileK / kChunkK; ++c)
-            tma_load_2d(bring + s * BST + c * NT * 128, &tm_b, &full[s], kt * kTileK + c * kChunkK, w.blk * NT,
-                        pol_b);
+            tma_load_2d(bring + s * BST + c * NT * 128, &tm_b, &full[s], token_x(kt, c), token_y(w.blk, NT), pol_b);
         }
         __syncwarp();
         if (++s == NS) {
@@ -445,7 +414,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     // values warp-uniform, an 8-MMA stage issues several times faster than from
     // a lone lane. Wrapping counters, precomputed descriptors, unrolled MMAs.
     const uint32_t idesc = idesc_f16(ACT, NT);
-    const uint32_t a_base = tmem + NACC * NT;
+    const uint32_t a_base = tmem + gemm_a_col(NACC, NT, 0);
     const uint64_t chunk_step = static_cast<uint64_t>((NT * 128) >> 4);  // next 64-wide K chunk
     int s = 0, slot = 0, uc = 0;
     uint32_t a_phase = 0;
@@ -455,7 +424,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
       const int acc = uc % NACC;
       if (!warp_wait_all(&accempty[acc], ((uc / NACC) & 1) ^ 1, abort_flag, a.status)) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem + acc * NT;
+      const uint32_t d_tmem = tmem + gemm_acc_col(acc, NT);
       bool ok = true;
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
         // afull implies the stage landed (the dequant warps waited on full[s])
@@ -580,7 +549,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
           }
           uint32_t outv[16];
           Dequant<BITS, ACT, SCL>::run(wv, zero[h >> 1], sbits[h >> 1], outv);
-          tmem_st16(tmem + t_lane + NACC * NT + cslot * kASlotCols + h * 16, outv);
+          tmem_st16(tmem + t_lane + gemm_a_col(NACC, NT, cslot) + h * 16, outv);
         }
         tmem_st_wait();
         tc_fence_before();
