@@ -42,6 +42,9 @@ from synthetic.workloads import make_routing  # noqa: E402
 METRIC = "fused W4A16 MoE layer tokens/s and achieved HBM GB/s (% of peak) vs batch M"
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+# one decode point of each other workload and the large int8 prefill batch,
+# reported beside the headline workload
+OTHER_POINTS = (("qwen2_57b", 8), ("deepseek_v3", 16), ("mixtral8x22b_w8", 8192))
 KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_defer.cuh", "common.cuh", "ptx.cuh", "host.cu")
 
 
@@ -57,6 +60,7 @@ def parse():
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-workloads", action="store_true")
     return p.parse_args()
 
 
@@ -399,6 +403,47 @@ def run_steps(call, flush, steps, ev_sets):
         call(ev_sets[i] if ev_sets is not None else None)
 
 
+def point_figures(w, wl, M, ids_np, per, ms_per_step, peaks, sustained=False):
+    """Algorithmic work, the dominant kernel's roofline and the whole-layer
+    figures of one measured point. ``per``: per-kernel times (ms) of the timed
+    pass; ``sustained``: compare a tensor-bound kernel with the sustained bf16
+    peak (a kernel timed inside a long step) instead of the burst peak."""
+    alg = algorithmic(wl, M, ids_np)
+    block = w.choose_block(M, wl.topk, wl.E)
+    exe = executed_work(wl, ids_np, block)
+    k1_ms, k2_ms = float(per[:, 2].mean()), float(per[:, 3].mean())
+    dom = ("gate_up_gemm", k1_ms, alg["gemm1_bytes"], alg["gemm1_flops"]) if k1_ms >= k2_ms else \
+        ("down_gemm", k2_ms, alg["gemm2_bytes"], alg["gemm2_flops"])
+    tc_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    t_hbm = dom[2] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = dom[3] / (tc_peak * 1e12)
+    if t_hbm >= t_tc:
+        achieved = dom[2] / (dom[1] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = dom[3] / (dom[1] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": achieved / tc_peak, "peak_kind": "sustained" if sustained else "burst"}
+    kname = gemm_kernel_name(w, wl, M, 1 if dom[0] == "gate_up_gemm" else 2)
+    roof.update({"traffic": ncu_traffic(f"{wl.name}/M={M}", kname), "kernel": dom[0],
+                 "kernel_ms": dom[1], "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
+                 if peaks["source"] == "measured" else "fallback",
+                 "algorithmic_bytes": dom[2], "algorithmic_flops": dom[3]})
+    layer_s = ms_per_step / 1e3
+    hbm = {"layer_algorithmic_bytes": alg["layer_bytes"], "layer_gbs": alg["layer_bytes"] / layer_s / 1e9,
+           "frac_of_peak": alg["layer_bytes"] / layer_s / 1e9 / peaks["hbm_gbs"],
+           "layer_tflops": alg["layer_flops"] / layer_s / 1e12,
+           "roofline_frac": max(alg["layer_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                                alg["layer_flops"] / (tc_peak * 1e12)) / layer_s,
+           "padded_slots": exe["padded_slots"], "routed_pairs": M * wl.topk,
+           "executed_tflops": exe["executed_flops"] / layer_s / 1e12,
+           "implementation_bytes": exe["implementation_bytes"]}
+    kernels = {"align": float(per[:, 0].mean()), "gather": float(per[:, 1].mean()),
+               "gate_up_gemm": k1_ms, "down_gemm": k2_ms, "combine": float(per[:, 4].mean())}
+    return alg, block, roof, hbm, kernels
+
+
 def ours_arm(args):
     import weight_quantized_moe_align_gb300 as w
 
@@ -420,15 +465,16 @@ def ours_arm(args):
     weights = make_expert_weights(wl, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def setup(Mx):
-        li = make_layer_inputs(wl, Mx, dev, weights)
-        ws = torch.empty(max(16, w.workspace_bytes(Mx, wl.H, wl.I, wl.E, wl.topk, wl.bits, wl.group_size)),
+    def setup(Mx, wlx=wl, weightsx=None):
+        weightsx = weights if weightsx is None else weightsx
+        li = make_layer_inputs(wlx, Mx, dev, weightsx)
+        ws = torch.empty(max(16, w.workspace_bytes(Mx, wlx.H, wlx.I, wlx.E, wlx.topk, wlx.bits, wlx.group_size)),
                          dtype=torch.uint8, device=dev)
-        out = torch.empty(Mx, wl.H, dtype=li.hidden.dtype, device=dev)
+        out = torch.empty(Mx, wlx.H, dtype=li.hidden.dtype, device=dev)
 
         def call(events):
             w.fused_moe(li.hidden, li.w13_q, li.w13_s, li.w13_z, li.w2_q, li.w2_s, li.w2_z, li.topk_ids,
-                        li.topk_w, wl.bits, wl.group_size, out=out, workspace=ws, events=events)
+                        li.topk_w, wlx.bits, wlx.group_size, out=out, workspace=ws, events=events)
         return li, ws, out, call
 
     def timed(call, steps, warmup):
@@ -442,15 +488,17 @@ def ours_arm(args):
         torch.cuda.synchronize()
         return np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(steps)])
 
-    def whole_steps(call, steps, warmup, sampler=None):
+    def whole_steps(call, steps, warmup, sampler=None, ranks=False):
         """Whole-layer times (ms) of the plain call, two events per step on the
-        launching stream; L2 flushed before each step outside the events."""
+        launching stream; L2 flushed before each step outside the events.
+        ``ranks``: bracket the timed steps with a barrier of all ranks (the
+        headline only; the other points run on rank 0 alone)."""
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for i in range(warmup):
             flush.zero_()
             call(None)
         torch.cuda.synchronize()
-        if dist:
+        if dist and ranks:
             dist.barrier()
         torch.cuda.synchronize()
         if sampler:
@@ -461,14 +509,14 @@ def ours_arm(args):
             call(None)
             evs[i][1].record()
         torch.cuda.synchronize()
-        if dist:
+        if dist and ranks:
             dist.barrier()
         clk = sampler.stop() if sampler else None
         return np.array([a.elapsed_time(b) for a, b in evs]), clk
 
     li, ws, out, call = setup(M)
     # ---- the timed region: whole layer calls
-    step_ms, clocks = whole_steps(call, args.steps, args.warmup, ClockSampler(local))
+    step_ms, clocks = whole_steps(call, args.steps, args.warmup, ClockSampler(local), ranks=True)
     total_ms = float(step_ms.sum())
     # ---- per-kernel breakdown (dominant kernel for the roofline), same steps count
     per = timed(call, args.steps, 3)
@@ -476,29 +524,8 @@ def ours_arm(args):
     ms_per_step = total_ms / args.steps
 
     ids_np = li.topk_ids.cpu().numpy()
-    alg = algorithmic(wl, M, ids_np)
-    block = w.choose_block(M, wl.topk, wl.E)
-    exe = executed_work(wl, ids_np, block)
-    k1_ms, k2_ms = float(per[:, 2].mean()), float(per[:, 3].mean())
-    dom = ("gate_up_gemm", k1_ms, alg["gemm1_bytes"], alg["gemm1_flops"]) if k1_ms >= k2_ms else \
-        ("down_gemm", k2_ms, alg["gemm2_bytes"], alg["gemm2_flops"])
-    t_hbm = dom[2] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = dom[3] / (peaks["bf16_tflops"] * 1e12)
-    if t_hbm >= t_tc:
-        achieved = dom[2] / (dom[1] / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"]}
-    else:
-        achieved = dom[3] / (dom[1] / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"]}
-    kname = gemm_kernel_name(w, wl, M, 1 if dom[0] == "gate_up_gemm" else 2)
-    roof.update({"traffic": ncu_traffic(f"{wl.name}/M={M}", kname), "kernel": dom[0],
-                 "kernel_ms": dom[1], "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
-                 if peaks["source"] == "measured" else "fallback",
-                 "algorithmic_bytes": dom[2], "algorithmic_flops": dom[3]})
+    alg, block, roof, hbm, kernels = point_figures(w, wl, M, ids_np, per, ms_per_step, peaks)
 
-    layer_s = ms_per_step / 1e3
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -506,16 +533,8 @@ def ours_arm(args):
         "step_us": step_stats(step_ms),
         "config": run_config(wl, M, world),
         "launch_config": {"block": block, "touched_experts": alg["touched"]},
-        "hbm": {"layer_algorithmic_bytes": alg["layer_bytes"], "layer_gbs": alg["layer_bytes"] / layer_s / 1e9,
-                "frac_of_peak": alg["layer_bytes"] / layer_s / 1e9 / peaks["hbm_gbs"],
-                "layer_tflops": alg["layer_flops"] / layer_s / 1e12,
-                "roofline_frac": max(alg["layer_bytes"] / (peaks["hbm_gbs"] * 1e9),
-                                     alg["layer_flops"] / (peaks["bf16_tflops"] * 1e12)) / layer_s,
-                "padded_slots": exe["padded_slots"], "routed_pairs": M * wl.topk,
-                "executed_tflops": exe["executed_flops"] / layer_s / 1e12,
-                "implementation_bytes": exe["implementation_bytes"]},
-        "kernels_ms": {"align": float(per[:, 0].mean()), "gather": float(per[:, 1].mean()),
-                       "gate_up_gemm": k1_ms, "down_gemm": k2_ms, "combine": float(per[:, 4].mean())},
+        "hbm": hbm,
+        "kernels_ms": kernels,
         "roofline": roof,
         "gpu_launches": 5 * args.steps * world,
         "launch": "the 4 launches after the align kernel are programmatic dependents of the one before "
@@ -547,6 +566,31 @@ def ours_arm(args):
             del lix, callx
         line["sweep"] = sweep
         line["routing"] = routing_times(w, wl, dev, flush, sorted({M, max(wl.m_sweep), 8192}), peaks)
+    if rank == 0 and not args.no_workloads:
+        # one point of each other workload, with its own roofline and clocks;
+        # only the experts its batch routes to are generated (the others are
+        # never read)
+        points = []
+        for name, Mx in OTHER_POINTS:
+            if name == wl.name:
+                continue
+            wlx = WORKLOADS[name]
+            wx = _sample_weights(wlx, Mx, dev, tokens=Mx)
+            lix, _, _, callx = setup(Mx, wlx, wx)
+            stx = max(10, min(args.steps, 50))
+            msx, clkx = whole_steps(callx, stx, max(3, args.warmup), ClockSampler(local))
+            perx = timed(callx, stx, 3)
+            mspx = float(msx.mean())
+            sustained = mspx > 5.0  # a long step: the tensor pipe runs under the power cap
+            ax, bx, roofx, hbmx, kx = point_figures(w, wlx, Mx, lix.topk_ids.cpu().numpy(), perx, mspx, peaks,
+                                                    sustained=sustained)
+            points.append({"config": run_config(wlx, Mx, world), "value": Mx / (mspx / 1e3), "unit": "tokens/s",
+                           "ms_per_step": mspx, "steps": stx, "step_us": step_stats(msx),
+                           "launch_config": {"block": bx, "touched_experts": ax["touched"]}, "hbm": hbmx,
+                           "kernels_ms": kx, "roofline": roofx, "clocks": clkx})
+            del wx, lix, callx
+            torch.cuda.empty_cache()
+        line["workloads"] = points
     if rank == 0 and not args.no_cpu_baseline:
         rate, desc, secs = time_oracle(li, 10.0)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
@@ -632,6 +676,16 @@ def e2e(w, wl, li, ws, flush, dev, steps):
         with torch.cuda.stream(stream):
             step()
 
+    # the same step through a plan made once for the weights (wna16_plan_create)
+    plan = w.Plan(li.w13_q, li.w13_s, li.w13_z, li.w2_q, li.w2_s, li.w2_z, wl.bits, wl.group_size, k,
+                  act_dtype=li.hidden.dtype)
+
+    def eager_plan():
+        with torch.cuda.stream(stream):
+            d_in.copy_(h_in, non_blocking=True)
+            plan(d_x, d_ids, d_w, d_out, ws, stream=stream)
+            h_out.copy_(d_out, non_blocking=True)
+
     with torch.cuda.stream(stream):
         step()  # warm-up on the capture stream
     stream.synchronize()
@@ -646,12 +700,17 @@ def e2e(w, wl, li, ws, flush, dev, steps):
     s_graph = timed(replay)
     graph_ok = bool(torch.equal(d_out, ref))
     s_eager = timed(eager)
+    s_plan = timed(eager_plan)
+    plan_ok = bool(torch.equal(d_out, ref))
     return {"value": M / s_graph, "unit": "tokens/s", "ms_per_step": s_graph * 1e3,
             "mode": "CUDA graph replay per step: H2D copy of the step's inputs, the layer's 5 launches, D2H copy",
             "h2d_bytes_per_step": nb, "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
             "graph_output_matches_eager": graph_ok,
             "eager": {"value": M / s_eager, "unit": "tokens/s", "ms_per_step": s_eager * 1e3,
-                      "mode": "fused_moe called from Python each step"}}
+                      "mode": "fused_moe called from Python each step"},
+            "eager_plan": {"value": M / s_plan, "unit": "tokens/s", "ms_per_step": s_plan * 1e3,
+                           "output_matches": plan_ok,
+                           "mode": "a plan made once for the weights, called from Python each step"}}
 
 
 def main():

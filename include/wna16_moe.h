@@ -116,6 +116,8 @@ wna16_status wna16_moe_align_block_size(const int32_t* topk_ids, int64_t M, int 
  * Block size the fused call uses when given block = 0, from the average routed
  * pairs per active expert, avg = M * topk / min(M * topk, E) (the routing
  * itself is not seen on the host):
+ *   E <= 16 and avg > 48: 128 (one block per expert; the MMA width and the
+ *     epilogue cover only the block's routed pairs, rounded up to 16);
  *   avg <= 64 (weight streaming dominates): the tile of 16, 32 or 64 tokens
  *     with the least estimated streaming cost, ceil(1.3 * avg / tile) passes
  *     over the expert's weights times the measured cost of one pass with that
@@ -184,11 +186,13 @@ size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, i
  *   block        align block size (0 = automatic), as in
  *                wna16_moe_align_block_size; it is also the GEMM token tile.
  *                Forced sizes other than the automatic choice are verified on
- *                the GPU for layers of up to 64 experts. With more experts they
- *                are accepted but unverified: one run of forced 32/64/128 on a
- *                256-expert layer at M = 256 ended in an unexplained launch
- *                failure, although wna16_check_launch_plan finds every index
- *                of those launch plans in bounds.
+ *                the GPU for layers of up to 8 experts. With more experts they
+ *                are accepted but unverified: sweeps of forced sizes much larger
+ *                than the routed pairs per expert ended twice in an unexplained
+ *                launch failure (256 experts at M = 256 with 32/64/128; 64
+ *                experts at M = 128 with 128, after clean calls of the same
+ *                configuration), although wna16_check_launch_plan finds every
+ *                index of those launch plans in bounds.
  *   split_k      K-splits of the down GEMM (0 = automatic, else 1..8).
  * Shapes: H a multiple of 64, I a multiple of 64, 1 <= topk <= E <= 256,
  * M*topk < 2^31. M = 0 returns WNA16_OK and launches nothing.
@@ -225,6 +229,34 @@ wna16_status wna16_fused_moe_timed(const void* hidden, wna16_dtype act_dtype, in
                                    const float* topk_weights, void* out, void* workspace,
                                    size_t workspace_bytes, int block, int split_k, void* stream,
                                    void* const* events);
+
+/*
+ * Plans: the fused layer for a fixed set of weights, called many times (a
+ * serving loop that does not capture CUDA graphs). wna16_plan_create checks
+ * the weight arguments once and encodes the weights' TMA descriptors once, in
+ * host memory; wna16_fused_moe_plan then runs the layer on a batch with only
+ * the batch-dependent work left on the host (the batch's checks, its launch
+ * plan, the two token-tile descriptors and the launches).
+ *   wna16_plan_create: arguments as wna16_fused_moe (weights: device pointers
+ *     that must stay valid and unchanged while the plan is used). Writes a
+ *     new plan to *plan (NULL on error). Makes no CUDA allocation, launch or
+ *     synchronization.
+ *   wna16_plan_destroy: frees a plan (NULL is ignored). Calls still running on
+ *     the GPU are not affected (they hold copies of the descriptors).
+ *   wna16_fused_moe_plan: wna16_fused_moe with the plan's weights; same
+ *     workspace size (wna16_fused_moe_workspace_bytes), errors and semantics.
+ * A plan may be used from several host threads at once (it is only read).
+ */
+typedef struct wna16_plan_t wna16_plan_t;
+
+wna16_status wna16_plan_create(wna16_dtype act_dtype, int64_t H, int64_t I, int E, int topk, const int32_t* w13_q,
+                               const void* w13_scales, const int32_t* w13_zeros, const int32_t* w2_q,
+                               const void* w2_scales, const int32_t* w2_zeros, wna16_dtype scale_dtype, int bits,
+                               int group_size, wna16_plan_t** plan);
+void wna16_plan_destroy(wna16_plan_t* plan);
+wna16_status wna16_fused_moe_plan(const wna16_plan_t* plan, const void* hidden, int64_t M, const int32_t* topk_ids,
+                                  const float* topk_weights, void* out, void* workspace, size_t workspace_bytes,
+                                  int block, int split_k, void* stream);
 
 /*
  * Size of the library-owned scratch area used by wna16_fused_moe_noalloc:
@@ -368,8 +400,10 @@ wna16_status wna16_convert_checkpoint(wna16_checkpoint format, const int32_t* qw
  *             and routed_weights [M, topk] fp32 (both required, written), then
  *             the layer on them; the topk_ids / topk_weights arguments are then
  *             ignored and may be NULL. Routing argument errors return before
- *             any launch; the routing launch precedes the five of the layer (the
- *             timed variant's events cover the layer's five).
+ *             any launch. Batches of up to 128 tokens are routed and aligned by
+ *             one launch (five launches in all); larger ones run the routing
+ *             launch before the layer's five. The timed variant's first event
+ *             is recorded before the align launch (routing included when fused).
  * A zero-initialized struct (or a NULL pointer) is the default layer. Both
  * bias pointers must be aligned to their 2-byte elements, the permutations to
  * 4 bytes.

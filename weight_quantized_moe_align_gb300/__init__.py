@@ -7,6 +7,7 @@ from .binding import (  # noqa: F401
     DEV_TIMEOUT,
     EXPORTED,
     PackedWeights,
+    Plan,
     act_order_prepare,
     WNA16Error,
     align_capacity,

@@ -35,6 +35,7 @@ EXPORTED = (
     "wna16_read_device_status", "wna16_status_string", "wna16_topk_routing", "wna16_fused_moe_ex",
     "wna16_fused_moe_prepacked_ex", "wna16_act_order_prepare", "wna16_convert_checkpoint",
     "wna16_check_wait_timeout", "wna16_noalloc_read_status", "wna16_check_launch_plan",
+    "wna16_plan_create", "wna16_plan_destroy", "wna16_fused_moe_plan",
 )
 
 _DTYPE = {torch.float16: 0, torch.bfloat16: 1}
@@ -139,6 +140,13 @@ def load() -> ctypes.CDLL:
     L.wna16_check_launch_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp,
                                           vp, c.c_int32, c.c_char_p, sz]
     L.wna16_check_launch_plan.restype = i64
+    L.wna16_plan_create.argtypes = [i32, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                    c.POINTER(vp)]
+    L.wna16_plan_create.restype = i32
+    L.wna16_plan_destroy.argtypes = [vp]
+    L.wna16_plan_destroy.restype = None
+    L.wna16_fused_moe_plan.argtypes = [vp, vp, i64, vp, vp, vp, vp, sz, i32, i32, vp]
+    L.wna16_fused_moe_plan.restype = i32
     L.wna16_status_string.argtypes = [i32]
     L.wna16_status_string.restype = c.c_char_p
     _lib = L
@@ -415,6 +423,72 @@ def noalloc_read_status(stream=None) -> int:
     if st not in (0, 5, 6, 7):
         _raise(st, "wna16_noalloc_read_status")
     return int(bits.value)
+
+
+class Plan:
+    """A ``wna16_plan_t``: the layer for one set of weights, its argument checks
+    and weight descriptors done once (see the header). ``plan(hidden, topk_ids,
+    topk_weights, out, workspace)`` runs the layer with only the batch's work
+    left on the host; the tensors must be contiguous CUDA tensors of the
+    documented shapes (checked once per distinct shape), and the weights must
+    stay alive and unchanged while the plan is used."""
+
+    def __init__(self, w13_q, w13_scales, w13_zeros, w2_q, w2_scales, w2_zeros, bits, group_size, topk,
+                 act_dtype=torch.float16):
+        E, twoI, _ = w13_q.shape
+        H = w2_q.shape[1]
+        self.E, self.I, self.H, self.topk, self.bits, self.group_size = E, twoI // 2, H, topk, bits, group_size
+        self.act_dtype = act_dtype
+        dev = w13_q.device
+        G1 = H if group_size == -1 else group_size
+        G2 = self.I if group_size == -1 else group_size
+        pf = 32 // bits
+        _check(w13_q, "w13_q", torch.int32, (E, 2 * self.I, H // pf), dev)
+        _check(w2_q, "w2_q", torch.int32, (E, H, self.I // pf), dev)
+        _check(w13_scales, "w13_scales", (torch.float16, torch.bfloat16), (E, H // G1, 2 * self.I), dev)
+        _check(w2_scales, "w2_scales", w13_scales.dtype, (E, self.I // G2, H), dev)
+        if (w13_zeros is None) != (w2_zeros is None):
+            raise ValueError("w13_zeros and w2_zeros must both be given or both be None")
+        if w13_zeros is not None:
+            _check(w13_zeros, "w13_zeros", torch.int32, (E, H // G1, 2 * self.I // pf), dev)
+            _check(w2_zeros, "w2_zeros", torch.int32, (E, self.I // G2, H // pf), dev)
+        self._keep = (w13_q, w13_scales, w13_zeros, w2_q, w2_scales, w2_zeros)
+        self._lib = load()
+        h = ctypes.c_void_p()
+        st = self._lib.wna16_plan_create(_DTYPE[act_dtype], H, self.I, E, topk, _ptr(w13_q), _ptr(w13_scales),
+                                         _ptr(w13_zeros), _ptr(w2_q), _ptr(w2_scales), _ptr(w2_zeros),
+                                         _DTYPE[w13_scales.dtype], bits, group_size, ctypes.byref(h))
+        _raise(st, "wna16_plan_create")
+        self._h = h
+        self._seen = set()
+        self._run = self._lib.wna16_fused_moe_plan
+
+    def workspace_bytes(self, M, block=0, split_k=0):
+        return workspace_bytes(M, self.H, self.I, self.E, self.topk, self.bits, self.group_size, block, split_k)
+
+    def __call__(self, hidden, topk_ids, topk_weights, out, workspace, block=0, split_k=0, stream=None):
+        M = hidden.shape[0]
+        key = (M, hidden.device, hidden.dtype, out.dtype, workspace.numel())
+        if key not in self._seen:
+            dev = hidden.device
+            _check(hidden, "hidden", self.act_dtype, (M, self.H), dev)
+            _check(topk_ids, "topk_ids", torch.int32, (M, self.topk), dev)
+            _check(topk_weights, "topk_weights", torch.float32, (M, self.topk), dev)
+            _check(out, "out", self.act_dtype, (M, self.H), dev)
+            _check(workspace, "workspace", torch.uint8, device=dev)
+            self._seen.add(key)
+        st = self._run(self._h, hidden.data_ptr(), M, topk_ids.data_ptr(), topk_weights.data_ptr(), out.data_ptr(),
+                       workspace.data_ptr(), workspace.numel(), block, split_k,
+                       (stream or torch.cuda.current_stream()).cuda_stream)
+        if st:
+            _raise(st, "wna16_fused_moe_plan")
+        return out
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.wna16_plan_destroy(h)
+            self._h = None
 
 
 class PackedWeights:

@@ -22,6 +22,8 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "plan.cuh"
+#include "routing_row.cuh"
 
 namespace wna16 {
 
@@ -29,11 +31,11 @@ constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
 constexpr int kMaxExperts = 256;
 
-__global__ void __launch_bounds__(kAlignThreads, 1)
-    moe_align_kernel(const int32_t* __restrict__ ids, int P, int E, int block, int cap,
-                     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
-                     int32_t* __restrict__ num_post_pad, int32_t* __restrict__ counts_out,
-                     int32_t* __restrict__ status, int32_t* __restrict__ slot_of_pair) {
+__device__ __forceinline__ void align_body(const int32_t* __restrict__ ids, int P, int E, int block, int cap,
+                                           int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                                           int32_t* __restrict__ num_post_pad, int32_t* __restrict__ counts_out,
+                                           int32_t* __restrict__ status, int32_t* __restrict__ slot_of_pair,
+                                           int32_t* __restrict__ block_rows) {
   __shared__ int cnt[kMaxExperts];
   __shared__ int off_end[kMaxExperts];      // exclusive end of each expert's padded segment
   __shared__ int run[kMaxExperts];          // next free slot of each expert
@@ -41,7 +43,6 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   __shared__ int total;
   __shared__ int bad;
 
-  grid_dep_launch();  // the gather may start its launch; it waits for this kernel's writes
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid < kMaxExperts) cnt[tid] = 0;
@@ -116,6 +117,12 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
       e = lo;
     }
     expert_ids[b] = e;
+    // routed pairs in the block (the rest is padding): the GEMMs size their
+    // MMAs and epilogues to it
+    if (block_rows) {
+      const int seg = e >= 0 ? off_end[e] - (cnt[e] + block - 1) / block * block : 0;  // e's first slot
+      block_rows[b] = e >= 0 ? rows_in_block(cnt[e], seg, start, block) : 0;
+    }
   }
   __syncthreads();  // orders the sentinel fill before the scatter below
 
@@ -153,6 +160,34 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
       for (int w = 0; w < kAlignWarps; ++w) wbase[w][x] = 0;
     __syncthreads();
   }
+}
+
+__global__ void __launch_bounds__(kAlignThreads, 1)
+    moe_align_kernel(const int32_t* __restrict__ ids, int P, int E, int block, int cap,
+                     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                     int32_t* __restrict__ num_post_pad, int32_t* __restrict__ counts_out,
+                     int32_t* __restrict__ status, int32_t* __restrict__ slot_of_pair,
+                     int32_t* __restrict__ block_rows) {
+  grid_dep_launch();  // the gather may start its launch; it waits for this kernel's writes
+  align_body(ids, P, E, block, cap, sorted_ids, expert_ids, num_post_pad, counts_out, status, slot_of_pair,
+             block_rows);
+}
+
+// Small batches routed on the device: the 32 warps first route the batch's
+// token rows (one warp per row, routing_row.cuh), writing the top-k ids and
+// weights, then the CTA aligns those ids; one launch instead of two.
+template <typename T, int VPL>
+__global__ void __launch_bounds__(kAlignThreads, 1)
+    moe_route_align_kernel(const T* __restrict__ logits, const routing::RouteArgs ra, int block, int cap,
+                           int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                           int32_t* __restrict__ num_post_pad, int32_t* __restrict__ counts_out,
+                           int32_t* __restrict__ status, int32_t* __restrict__ slot_of_pair,
+                           int32_t* __restrict__ block_rows) {
+  grid_dep_launch();
+  for (int row = threadIdx.x >> 5; row < ra.M; row += kAlignWarps) routing::route_row<T, VPL>(logits, ra, row);
+  __syncthreads();  // the routed ids (global memory) are visible to the whole CTA
+  align_body(ra.ids, ra.M * ra.topk, ra.E, block, cap, sorted_ids, expert_ids, num_post_pad, counts_out, status,
+             slot_of_pair, block_rows);
 }
 
 // Copies the hidden row of every routed pair to its expert-sorted slot:
@@ -299,9 +334,38 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* num_post_pad, int32_t* counts,
-                         int32_t* status, int32_t* slot_of_pair, cudaStream_t stream) {
+                         int32_t* status, int32_t* slot_of_pair, int32_t* block_rows, cudaStream_t stream) {
   moe_align_kernel<<<1, kAlignThreads, 0, stream>>>(ids, P, E, block, cap, sorted_ids, expert_ids,
-                                                    num_post_pad, counts, status, slot_of_pair);
+                                                    num_post_pad, counts, status, slot_of_pair, block_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_align(const void* logits, int logits_dtype, int M, int E, int topk, int sigmoid, int renorm,
+                               int n_groups, int topk_groups, int32_t* routed_ids, float* routed_weights, int block,
+                               int cap, int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_pad,
+                               int32_t* counts, int32_t* status, int32_t* slot_of_pair, int32_t* block_rows,
+                               cudaStream_t stream) {
+  const routing::RouteArgs ra{M, E, topk, sigmoid, renorm, n_groups, n_groups > 1 ? topk_groups : 1, routed_ids,
+                              routed_weights};
+  const int vpl = (E + 31) / 32;
+#define WNA16_ROUTE_ALIGN(T, V)                                                                               \
+  moe_route_align_kernel<T, V><<<1, kAlignThreads, 0, stream>>>(static_cast<const T*>(logits), ra, block, cap, \
+                                                                sorted_ids, expert_ids, num_post_pad, counts,  \
+                                                                status, slot_of_pair, block_rows)
+#define WNA16_ROUTE_ALIGN_T(T)            \
+  if (vpl <= 1) WNA16_ROUTE_ALIGN(T, 1);  \
+  else if (vpl <= 2) WNA16_ROUTE_ALIGN(T, 2); \
+  else if (vpl <= 4) WNA16_ROUTE_ALIGN(T, 4); \
+  else WNA16_ROUTE_ALIGN(T, 8)
+  if (logits_dtype == 2) {
+    WNA16_ROUTE_ALIGN_T(float);
+  } else if (logits_dtype == 0) {
+    WNA16_ROUTE_ALIGN_T(__half);
+  } else {
+    WNA16_ROUTE_ALIGN_T(__nv_bfloat16);
+  }
+#undef WNA16_ROUTE_ALIGN_T
+#undef WNA16_ROUTE_ALIGN
   return cudaGetLastError();
 }
 

@@ -72,6 +72,7 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 struct GemmArgs {
   const int32_t* sorted_ids;   // [cap]
   const int32_t* expert_ids;   // [cap / block]
+  const int32_t* block_rows;   // [cap / block] routed pairs in each block (the rest is padding)
   const int32_t* num_post_pad; // [1]
   const float* topk_w;         // [P] (down GEMM)
   void* out;                   // act cache [cap, I] (gate/up) or slab [split, P, H] fp32 (down)

@@ -195,6 +195,8 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
                                               uint32_t acc_phase, uint64_t* accfull, uint64_t* accempty,
                                               volatile int* abort_flag, int q, int lane) {
   const int NT = a.block;
+  // token columns the unit's MMAs wrote: the block's routed pairs, rounded up to 16
+  const int ncols = trimmed_n(a.block_rows[w.blk], NT);
   if (!warp_wait_all(&accfull[acc], acc_phase, abort_flag, a.status)) return false;
   tc_fence_after();
   const uint32_t t_base = tmem + ((q * 32) << 16) + gemm_acc_col(acc, NT);
@@ -227,7 +229,7 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
       if (has_bias) bias = bias_of<ACT>(a, e, h);
     }
   }
-  for (int c0 = 0; c0 < NT; c0 += 16) {
+  for (int c0 = 0; c0 < ncols; c0 += 16) {
     uint32_t v[16];
     tmem_ld16(t_base + c0, v);
     tmem_ld_wait();
@@ -413,7 +415,6 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     // The whole warp runs the loop and one elected lane issues: with the loop
     // values warp-uniform, an 8-MMA stage issues several times faster than from
     // a lone lane. Wrapping counters, precomputed descriptors, unrolled MMAs.
-    const uint32_t idesc = idesc_f16(ACT, NT);
     const uint32_t a_base = tmem + gemm_a_col(NACC, NT, 0);
     const uint64_t chunk_step = static_cast<uint64_t>((NT * 128) >> 4);  // next 64-wide K chunk
     int s = 0, slot = 0, uc = 0;
@@ -425,6 +426,8 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
       if (!warp_wait_all(&accempty[acc], ((uc / NACC) & 1) ^ 1, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem + gemm_acc_col(acc, NT);
+      // MMA width: the block's routed pairs rounded up to 16 (padding skipped)
+      const uint32_t idesc = idesc_f16(ACT, trimmed_n(a.block_rows[w.blk], NT));
       bool ok = true;
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
         // afull implies the stage landed (the dequant warps waited on full[s])

@@ -26,7 +26,15 @@ cudaError_t launch_gemm_defer_var(int bits, int act, int scl, int gemm, dim3 gri
 
 cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* num_post_pad, int32_t* counts,
-                         int32_t* status, int32_t* slot_of_pair, cudaStream_t stream);
+                         int32_t* status, int32_t* slot_of_pair, int32_t* block_rows, cudaStream_t stream);
+// Routing of a small batch (M <= kRouteAlignRows rows) and its align in one
+// launch of one CTA; logits_dtype: 0 fp16, 1 bf16, 2 fp32.
+constexpr int kRouteAlignRows = 128;
+cudaError_t launch_route_align(const void* logits, int logits_dtype, int M, int E, int topk, int sigmoid, int renorm,
+                               int n_groups, int topk_groups, int32_t* routed_ids, float* routed_weights, int block,
+                               int cap, int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_pad,
+                               int32_t* counts, int32_t* status, int32_t* slot_of_pair, int32_t* block_rows,
+                               cudaStream_t stream);
 // Expert-sorted copy of the hidden rows; with `xs` also the deferred-scale
 // token sums [H/128 stages][4 parts][cap]. It also zeroes the `zero_n` 32-bit
 // words at each `zero_ptr` (token-sum parts of a stage half with no K

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "wna16_moe.h"
 #include "common.cuh"
@@ -103,7 +104,7 @@ wna16_status wna16_moe_align_block_size(const int32_t* topk_ids, int64_t M, int 
     return WNA16_ERR_INVALID_ARG;
   const int64_t cap = capacity(P, E, block);
   if (launch_align(topk_ids, static_cast<int>(P), E, block, static_cast<int>(cap), sorted_ids, expert_ids,
-                   num_tokens_post_padded, expert_counts, device_status, nullptr,
+                   num_tokens_post_padded, expert_counts, device_status, nullptr, nullptr,
                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return WNA16_ERR_CUDA;
   return WNA16_OK;
@@ -129,7 +130,8 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
                        const void* w13_pack, const void* w2_pack, int pack_zeros, wna16_dtype scale_dtype,
                        int bits, int group_size, const int32_t* topk_ids, const float* topk_weights, void* out,
                        void* workspace, size_t workspace_bytes, int block, int split_k, void* stream,
-                       void* const* events, const wna16_moe_options* opt) {
+                       void* const* events, const wna16_moe_options* opt,
+                       const EncodedMaps* weight_maps = nullptr) {
   if (act_dtype != WNA16_F16 && act_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
   if (opt) {
     if (opt->activation != WNA16_ACT_SILU && opt->activation != WNA16_ACT_SWIGLU_CLAMP) return WNA16_ERR_INVALID_ARG;
@@ -191,19 +193,36 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
     if (events && events[i]) return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
     return true;
   };
+  // weight maps: encoded once by a plan (wna16_plan_create), else here
   EncodedMaps m1, m2;
-  if (!encode_maps(&m1, p.m1, !packed) || !encode_maps(&m2, p.m2, !packed)) return WNA16_ERR_CUDA;
-
-  if (routed) {
-    // its own argument checks run before its launch, the first of this call
-    const wna16_status rs = wna16_topk_routing(opt->router_logits, opt->logits_dtype, M, E, topk, opt->scoring,
-                                               opt->renormalize, opt->n_groups, opt->topk_groups, opt->routed_ids,
-                                               opt->routed_weights, stream);
-    if (rs != WNA16_OK) return rs;
+  const bool fresh = weight_maps == nullptr;
+  if (!encode_maps(&m1, p.m1, !packed && fresh) || !encode_maps(&m2, p.m2, !packed && fresh)) return WNA16_ERR_CUDA;
+  if (!fresh) {
+    m1.q = weight_maps[0].q, m1.s = weight_maps[0].s, m1.z = weight_maps[0].z;
+    m2.q = weight_maps[1].q, m2.s = weight_maps[1].s, m2.z = weight_maps[1].z;
   }
-  if (!mark(0) || launch_align(topk_ids, p.P, E, p.B, static_cast<int>(p.cap), sorted, experts, npp, counts, status,
-                               slot_of_pair, s) != cudaSuccess)
-    return WNA16_ERR_CUDA;
+
+  int32_t* block_rows = reinterpret_cast<int32_t*>(ws + p.L.block_rows);
+  if (routed && M <= kRouteAlignRows) {
+    // a small batch is routed and aligned by one launch
+    if (!mark(0) || launch_route_align(opt->router_logits, opt->logits_dtype, static_cast<int>(M), E, topk,
+                                       opt->scoring == WNA16_SCORE_SIGMOID ? 1 : 0, opt->renormalize ? 1 : 0,
+                                       opt->n_groups, opt->topk_groups, opt->routed_ids, opt->routed_weights, p.B,
+                                       static_cast<int>(p.cap), sorted, experts, npp, counts, status, slot_of_pair,
+                                       block_rows, s) != cudaSuccess)
+      return WNA16_ERR_CUDA;
+  } else {
+    if (routed) {
+      // its own argument checks ran above; its launch is the first of this call
+      const wna16_status rs = wna16_topk_routing(opt->router_logits, opt->logits_dtype, M, E, topk, opt->scoring,
+                                                 opt->renormalize, opt->n_groups, opt->topk_groups, opt->routed_ids,
+                                                 opt->routed_weights, stream);
+      if (rs != WNA16_OK) return rs;
+    }
+    if (!mark(0) || launch_align(topk_ids, p.P, E, p.B, static_cast<int>(p.cap), sorted, experts, npp, counts,
+                                 status, slot_of_pair, block_rows, s) != cudaSuccess)
+      return WNA16_ERR_CUDA;
+  }
   float* zero1 = p.zero1_n ? ws_words + p.zero1_off : nullptr;
   float* zero2 = p.zero2_n ? ws_words + p.zero2_off : nullptr;
   float* cnt1 = p.cnt1_n ? ws_words + p.cnt1_off : nullptr;
@@ -303,6 +322,79 @@ wna16_status wna16_fused_moe(const void* hidden, wna16_dtype act_dtype, int64_t 
   return wna16_fused_moe_timed(hidden, act_dtype, M, H, I, E, topk, w13_q, w13_scales, w13_zeros, w2_q,
                                w2_scales, w2_zeros, scale_dtype, bits, group_size, topk_ids, topk_weights,
                                out, workspace, workspace_bytes, block, split_k, stream, nullptr);
+}
+
+}  // extern "C"
+
+struct wna16_plan_t {
+  wna16_dtype act_dtype, scale_dtype;
+  int64_t H, I;
+  int E, topk, bits, group_size;
+  const int32_t *w13_q, *w13_zeros, *w2_q, *w2_zeros;
+  const void *w13_scales, *w2_scales;
+  EncodedMaps maps[2];  // weight maps of the gate/up and down projections
+};
+
+extern "C" {
+
+wna16_status wna16_plan_create(wna16_dtype act_dtype, int64_t H, int64_t I, int E, int topk, const int32_t* w13_q,
+                               const void* w13_scales, const int32_t* w13_zeros, const int32_t* w2_q,
+                               const void* w2_scales, const int32_t* w2_zeros, wna16_dtype scale_dtype, int bits,
+                               int group_size, wna16_plan_t** plan) {
+  if (!plan) return WNA16_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (act_dtype != WNA16_F16 && act_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
+  if (scale_dtype != WNA16_F16 && scale_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
+  if (!w13_q || !w13_scales || !w2_q || !w2_scales) return WNA16_ERR_INVALID_ARG;
+  if ((w13_zeros == nullptr) != (w2_zeros == nullptr)) return WNA16_ERR_INVALID_ARG;
+  const void* ptrs[] = {w13_q, w13_scales, w13_zeros, w2_q, w2_scales, w2_zeros};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return WNA16_ERR_INVALID_ARG;
+  // the weight maps do not depend on the batch: plan a one-token call with a
+  // stand-in workspace to describe them
+  LayerPlan lp;
+  uint8_t* const stand_in = reinterpret_cast<uint8_t*>(uintptr_t(1) << 40);
+  const wna16_status st = plan_layer(act_dtype, 1, H, I, E, topk, w13_q, w13_scales, w13_zeros, w2_q, w2_scales,
+                                     w2_zeros, nullptr, nullptr, 0, scale_dtype, bits, group_size, nullptr, stand_in,
+                                     ~size_t(0) >> 2, 0, 0, false, nullptr, sm_count(), &lp);
+  if (st != WNA16_OK) return st;
+  wna16_plan_t* p = new (std::nothrow) wna16_plan_t();
+  if (!p) return WNA16_ERR_UNSUPPORTED;
+  p->act_dtype = act_dtype;
+  p->scale_dtype = scale_dtype;
+  p->H = H;
+  p->I = I;
+  p->E = E;
+  p->topk = topk;
+  p->bits = bits;
+  p->group_size = group_size;
+  p->w13_q = w13_q;
+  p->w13_scales = w13_scales;
+  p->w13_zeros = w13_zeros;
+  p->w2_q = w2_q;
+  p->w2_scales = w2_scales;
+  p->w2_zeros = w2_zeros;
+  std::memset(p->maps, 0, sizeof(p->maps));
+  if (!encode_map(&p->maps[0].q, lp.m1.q) || !encode_map(&p->maps[0].s, lp.m1.s) ||
+      (lp.m1.has_z && !encode_map(&p->maps[0].z, lp.m1.z)) || !encode_map(&p->maps[1].q, lp.m2.q) ||
+      !encode_map(&p->maps[1].s, lp.m2.s) || (lp.m2.has_z && !encode_map(&p->maps[1].z, lp.m2.z))) {
+    delete p;
+    return WNA16_ERR_CUDA;
+  }
+  *plan = p;
+  return WNA16_OK;
+}
+
+void wna16_plan_destroy(wna16_plan_t* plan) { delete plan; }
+
+wna16_status wna16_fused_moe_plan(const wna16_plan_t* plan, const void* hidden, int64_t M, const int32_t* topk_ids,
+                                  const float* topk_weights, void* out, void* workspace, size_t workspace_bytes,
+                                  int block, int split_k, void* stream) {
+  if (!plan) return WNA16_ERR_INVALID_ARG;
+  const wna16_plan_t& p = *plan;
+  return run_layer(hidden, p.act_dtype, M, p.H, p.I, p.E, p.topk, p.w13_q, p.w13_scales, p.w13_zeros, p.w2_q,
+                   p.w2_scales, p.w2_zeros, nullptr, nullptr, 0, p.scale_dtype, p.bits, p.group_size, topk_ids,
+                   topk_weights, out, workspace, workspace_bytes, block, split_k, stream, nullptr, nullptr, p.maps);
 }
 
 wna16_status wna16_read_device_status(const void* status_word, int32_t* bits_out, void* stream) {

@@ -43,18 +43,30 @@ int64_t expected_blocks(int64_t M, int topk, int E, int block) {
   return active * ((avg + block - 1) / block);
 }
 
-// K split of a GEMM launch: only when the units do not fill the persistent CTA
-// slots, then as many splits as fit (at most 8, keeping >= 8 K stages per
-// split). Finer splits that merely even out the rounds were measured slower:
-// every unit boundary stalls the dequant chain (accumulator handoff, epilogue,
-// and for the gate/up GEMM the partial-sum exchange).
+// K split of a GEMM launch. The persistent CTAs take the units in rounds, so
+// a launch lasts about ceil(units * s / slots) unit times, and a unit of split
+// s lasts kt/s stages plus a fixed cost at its boundary (accumulator handoff,
+// epilogue, the split's partial-sum exchange), taken as kUnitCost stages. The
+// split with the least such time wins (ties to fewer splits), at most 8 and
+// keeping >= 8 stages per split. One round of unsplit units that leaves half
+// the slots idle (two routed experts at decode) is where it pays.
+constexpr double kUnitCost = 4.0;
+
 int choose_split(int64_t units, int kt_total, int ctas_per_sm, int sms) {
   const int64_t slots = static_cast<int64_t>(sms) * ctas_per_sm;
-  if (units >= slots) return 1;
-  int s = static_cast<int>(slots / std::max<int64_t>(units, 1));
-  s = std::min(s, 8);
-  s = std::min(s, std::max(1, kt_total / 8));
-  return std::max(s, 1);
+  if (units <= 0) return 1;
+  const int max_s = std::max(1, std::min(8, kt_total / 8));
+  int best = 1;
+  double best_t = 1e300;
+  for (int s = 1; s <= max_s; ++s) {
+    const double rounds = static_cast<double>((units * s + slots - 1) / slots);
+    const double t = rounds * (static_cast<double>(kt_total) / s + kUnitCost);
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = s;
+    }
+  }
+  return best;
 }
 
 // Gate/up (rows = 2I): codes [E*2 halves, I, K/pf] box {128/pf, 64, 2} (gate
@@ -161,6 +173,13 @@ int choose_block_impl(int64_t M, int topk, int E) {
   if (P <= 0) return 16;
   const int64_t active = std::min<int64_t>(P, E);
   const double avg = static_cast<double>(P) / static_cast<double>(active);  // pairs per active expert
+  // Few experts with more than 48 pairs each: one 128-token block per expert.
+  // The general kernel trims its MMA width to the block's pairs, so the
+  // padding costs no tensor work, and each expert's weights are dequantized
+  // once instead of twice (8-expert layer at 64 pairs per expert: 283 against
+  // 315 us with 64-token blocks). Layers with more experts keep the choices
+  // below: larger blocks on them are unverified (see the header).
+  if (E <= 16 && avg > 48.0) return 128;
   if (avg <= 64.0) {
     // Weight streaming dominates: every token block of an expert streams the
     // expert's whole weights once. Pick the tile with the fewest streaming
@@ -275,6 +294,7 @@ WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, 
   w.status = take(4);
   w.sorted = take(static_cast<size_t>(cap) * 4);
   w.experts = take(static_cast<size_t>(cap / block) * 4);
+  w.block_rows = take(static_cast<size_t>(cap / block) * 4);
   w.npp = take(4);
   w.counts = take(static_cast<size_t>(E) * 4);
   w.slot_of_pair = take(static_cast<size_t>(P) * 4);
@@ -374,6 +394,7 @@ wna16_status plan_layer(wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I, 
   GemmArgs& a1 = p.a1;
   a1.sorted_ids = reinterpret_cast<int32_t*>(ws + p.L.sorted);
   a1.expert_ids = reinterpret_cast<int32_t*>(ws + p.L.experts);
+  a1.block_rows = reinterpret_cast<int32_t*>(ws + p.L.block_rows);
   a1.num_post_pad = reinterpret_cast<int32_t*>(ws + p.L.npp);
   a1.topk_w = topk_weights;
   a1.out = ws + p.L.act;

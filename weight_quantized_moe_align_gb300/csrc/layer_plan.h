@@ -35,7 +35,8 @@ wna16_status resolve(int64_t M, int64_t H, int64_t I, int E, int topk, int bits,
                      int split_k, int sms, Resolved* r);
 
 struct WsLayout {
-  size_t status, sorted, experts, npp, counts, slot_of_pair, x_sorted, act, slab, xs1, xs2, part1, cnt1, total;
+  size_t status, sorted, experts, block_rows, npp, counts, slot_of_pair, x_sorted, act, slab, xs1, xs2, part1, cnt1,
+      total;
 };
 WsLayout ws_layout(int64_t M, int64_t H, int64_t I, int E, int topk, int block, int split, int split1);
 

@@ -44,6 +44,21 @@ WNA16_HD int active_blocks(int num_post_pad, int nt, int max_blocks) {
   return nb < 0 ? 0 : (nb > max_blocks ? max_blocks : nb);
 }
 
+// Routed pairs in the block starting at slot `start` of an expert whose cnt
+// pairs begin at slot seg (its padded segment holds them first, then padding).
+WNA16_HD int rows_in_block(int cnt, int seg, int start, int block) {
+  const int rows = cnt - (start - seg);
+  return rows < 0 ? 0 : (rows > block ? block : rows);
+}
+
+// MMA width (tokens) of a block holding `rows` routed pairs in a tile of nt:
+// the rows rounded up to the MMA's N granule of 16; the padding past it is
+// neither multiplied nor written back.
+WNA16_HD int trimmed_n(int rows, int nt) {
+  const int n = (rows + 15) & ~15;
+  return n < 16 ? 16 : (n > nt ? nt : n);
+}
+
 // Blocks below the padded total always hold a valid expert id; anything else
 // is mapped to expert 0 so that no address is formed from it.
 WNA16_HD int clamp_expert(int e, int E) { return (e >= 0 && e < E) ? e : 0; }

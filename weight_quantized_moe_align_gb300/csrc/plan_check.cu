@@ -126,6 +126,31 @@ extern "C" int64_t wna16_check_launch_plan(int64_t M, int64_t H, int64_t I, int 
   for (int b = 0; b < nb; ++b)
     if (expert_ids[b] < 0 || expert_ids[b] >= E) c.fail("expert_ids[%d] = %d below the padded total", b, expert_ids[b]);
 
+  // rows per block as the align kernel computes them (from each expert's count
+  // and segment start), checked against the align output: the routed pairs
+  // lead each block and the padding follows
+  std::vector<int> cnt(E, 0), seg(E, -1), block_rows(p.max_blocks, 0);
+  for (int pr = 0; pr < P; ++pr)
+    if (topk_ids[pr] >= 0 && topk_ids[pr] < E) ++cnt[topk_ids[pr]];
+  for (int b = 0; b < nb; ++b) {
+    const int e = expert_ids[b];
+    if (e >= 0 && e < E && seg[e] < 0) seg[e] = b * B;
+  }
+  for (int b = 0; b < nb; ++b) {
+    const int e = expert_ids[b];
+    if (e < 0 || e >= E) continue;
+    block_rows[b] = rows_in_block(cnt[e], seg[e], b * B, B);
+    for (int col = 0; col < B; ++col) {
+      const int pid = sorted_ids[static_cast<int64_t>(b) * B + col];
+      const bool routed = pid >= 0 && pid < P;
+      if (routed != (col < block_rows[b])) {
+        c.fail("block %d: column %d %s, but the block holds %d routed pairs first", b, col,
+               routed ? "routed" : "padding", block_rows[b]);
+        break;
+      }
+    }
+  }
+
   // ------------------------------------------------------------ gather
   std::vector<int> slot_of_pair(P, -1);
   for (int64_t i = 0; i < cap; ++i) {
@@ -164,6 +189,7 @@ extern "C" int64_t wna16_check_launch_plan(int64_t M, int64_t H, int64_t I, int 
     GemmArgs a = gemm == 1 ? p.a1 : p.a2;
     a.sorted_ids = sorted_ids;
     a.expert_ids = expert_ids;
+    a.block_rows = block_rows.data();
     const GemmMaps& maps = gemm == 1 ? p.m1 : p.m2;
     const unsigned grid = gemm == 1 ? p.grid1 : p.grid2;
     const size_t smem = gemm == 1 ? p.smem1 : p.smem2;
@@ -250,14 +276,17 @@ extern "C" int64_t wna16_check_launch_plan(int64_t M, int64_t H, int64_t I, int 
             check_box(c, maps.x, xc, "token sums", gemm, static_cast<int>(u), kt);
           }
         }
-        // epilogue
+        // epilogue: the general kernel writes the block's routed columns
+        // rounded up to 16, the deferred-scale kernel all of them
+        const int ncols = p.defer ? B : trimmed_n(a.block_rows[w.blk], B);
+        if (ncols < block_rows[w.blk]) c.fail("GEMM %d: block %d writes %d of its %d routed columns", gemm, w.blk, ncols, block_rows[w.blk]);
         if (gemm == 1) {
           for (int q = 0; q < 4; ++q)
             for (int lane = 0; lane < 32; ++lane) {
               const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
               const int fp = bits == 4 ? permute_k8(f) : f;
               if (f >= a.I) c.fail("GEMM 1: feature %d of tile %d past I", f, w.tile);
-              for (int col = 0; col < B; ++col) {
+              for (int col = 0; col < ncols; ++col) {
                 if (act_index(w.blk, B, col, a.I, fp) >= act_elems)
                   c.fail("GEMM 1: act cache element of block %d column %d feature %d past the act cache", w.blk, col, fp);
               }
@@ -278,7 +307,7 @@ extern "C" int64_t wna16_check_launch_plan(int64_t M, int64_t H, int64_t I, int 
               }
             }
         } else {
-          for (int col = 0; col < B; ++col) {
+          for (int col = 0; col < ncols; ++col) {
             const int64_t si = static_cast<int64_t>(w.blk) * B + col;
             if (si >= cap) {
               c.fail("GEMM 2: sorted_ids read %lld past the capacity", (long long)si);
