@@ -404,6 +404,14 @@ wna16_status wna16_convert_checkpoint(wna16_checkpoint format, const int32_t* qw
  *             one launch (five launches in all); larger ones run the routing
  *             launch before the layer's five. The timed variant's first event
  *             is recorded before the align launch (routing included when fused).
+ *   atomic_reduce (vLLM PR #14138's use_atomic_add, for comparison): != 0
+ *             makes the down GEMM add each (token, slot) row, already scaled
+ *             by its top-k weight, into an fp32 [M, H] accumulator with
+ *             atomicAdd (all slots and K splits of a token into one row; the
+ *             addition order, and so the last bits, varies from run to run),
+ *             and the last launch only rounds it. The default (0) writes each
+ *             row once to its own place and adds them in slot order (the
+ *             result is reproducible). Not combined with act-order weights.
  * A zero-initialized struct (or a NULL pointer) is the default layer. Both
  * bias pointers must be aligned to their 2-byte elements, the permutations to
  * 4 bytes.
@@ -427,6 +435,7 @@ typedef struct {
   int topk_groups;
   int32_t* routed_ids;
   float* routed_weights;
+  int atomic_reduce;
 } wna16_moe_options;
 
 /*

@@ -240,3 +240,21 @@ def test_deterministic_across_calls():
     a = run_layer(li, block=16).clone()
     b = run_layer(li, block=16)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("block", [16, 32, 64])
+@pytest.mark.parametrize("split_k", [1, 2, 3])
+def test_atomic_down_reduction(block, split_k):
+    # the fp32-atomic variant of the down GEMM's reduction (slots and K splits
+    # added into one [M, H] row per token): within the tolerance of the oracle
+    # and of the ordered reduction, though not bit-reproducible
+    wl = small(H=512, I=768, group_size=128, E=6, topk=3)
+    li = make_layer_inputs(wl, 37).to(DEV)
+    ordered = run_layer(li, block=block, split_k=split_k).clone()
+    y = w.fused_moe(li.hidden, li.w13_q, li.w13_s, li.w13_z, li.w2_q, li.w2_s, li.w2_z, li.topk_ids, li.topk_w,
+                    wl.bits, wl.group_size, block=block, split_k=split_k, atomic_reduce=True)
+    torch.cuda.synchronize()
+    ref = bits_to_f64(oracle.fused_moe_grouped(oracle_layer_dict(li)), wl.act_dtype)
+    g = bits_to_f64(halfbits(y), wl.act_dtype)
+    assert max_rel_err(g, ref) <= TOL
+    assert max_rel_err(g, bits_to_f64(halfbits(ordered), wl.act_dtype)) <= TOL

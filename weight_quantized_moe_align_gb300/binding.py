@@ -50,15 +50,18 @@ class MoeOptions(ctypes.Structure):
                 ("swiglu_limit", ctypes.c_float), ("w13_perm", ctypes.c_void_p), ("w2_inv_perm", ctypes.c_void_p),
                 ("router_logits", ctypes.c_void_p), ("logits_dtype", ctypes.c_int), ("scoring", ctypes.c_int),
                 ("renormalize", ctypes.c_int), ("n_groups", ctypes.c_int), ("topk_groups", ctypes.c_int),
-                ("routed_ids", ctypes.c_void_p), ("routed_weights", ctypes.c_void_p)]
+                ("routed_ids", ctypes.c_void_p), ("routed_weights", ctypes.c_void_p),
+                ("atomic_reduce", ctypes.c_int)]
 
 
 _ACTIVATION = {"silu": 0, "swiglu_clamp": 1}
 
 
-def _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu, w13_perm=None, w2_inv_perm=None):
+def _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu, w13_perm=None, w2_inv_perm=None,
+             atomic_reduce=False):
     """A MoeOptions for the given variant, or None for the default layer."""
-    if w13_bias is None and w2_bias is None and activation == "silu" and w13_perm is None and w2_inv_perm is None:
+    if (w13_bias is None and w2_bias is None and activation == "silu" and w13_perm is None and w2_inv_perm is None
+            and not atomic_reduce):
         return None
     if activation not in _ACTIVATION:
         raise ValueError(f"activation must be one of {tuple(_ACTIVATION)}")
@@ -72,11 +75,13 @@ def _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu, w13_perm=No
     if w2_inv_perm is not None:
         _check(w2_inv_perm, "w2_inv_perm", torch.int32, (E, I), dev)
     alpha, beta, limit = swiglu
-    return MoeOptions(None if w13_bias is None else w13_bias.data_ptr(),
-                      None if w2_bias is None else w2_bias.data_ptr(), _ACTIVATION[activation],
-                      float(alpha), float(beta), float(limit),
-                      None if w13_perm is None else w13_perm.data_ptr(),
-                      None if w2_inv_perm is None else w2_inv_perm.data_ptr())
+    opt = MoeOptions(None if w13_bias is None else w13_bias.data_ptr(),
+                     None if w2_bias is None else w2_bias.data_ptr(), _ACTIVATION[activation],
+                     float(alpha), float(beta), float(limit),
+                     None if w13_perm is None else w13_perm.data_ptr(),
+                     None if w2_inv_perm is None else w2_inv_perm.data_ptr())
+    opt.atomic_reduce = 1 if atomic_reduce else 0
+    return opt
 
 
 class WNA16Error(RuntimeError):
@@ -259,7 +264,7 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
               stream=None, events=None, w13_bias: Optional[torch.Tensor] = None,
               w2_bias: Optional[torch.Tensor] = None, activation: str = "silu",
               swiglu=(1.702, 1.0, 7.0), w13_perm: Optional[torch.Tensor] = None,
-              w2_inv_perm: Optional[torch.Tensor] = None) -> torch.Tensor:
+              w2_inv_perm: Optional[torch.Tensor] = None, atomic_reduce: bool = False) -> torch.Tensor:
     """The fused layer (see include/wna16_moe.h). Returns ``out`` [M, H].
 
     ``events``: optional list of 6 ``torch.cuda.Event`` (or None; each must
@@ -303,7 +308,7 @@ def fused_moe(hidden: torch.Tensor, w13_q: torch.Tensor, w13_scales: torch.Tenso
             _ptr(w13_zeros), _ptr(w2_q), _ptr(w2_scales), _ptr(w2_zeros), _DTYPE[w13_scales.dtype], bits,
             group_size, _ptr(topk_ids), _ptr(topk_weights), _ptr(out), _ptr(workspace),
             workspace.numel(), block, split_k, _stream(stream))
-    opt = _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu, w13_perm, w2_inv_perm)
+    opt = _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu, w13_perm, w2_inv_perm, atomic_reduce)
     if opt is not None:
         arr = None
         if events is not None:
@@ -530,7 +535,7 @@ def fused_moe_prepacked(hidden: torch.Tensor, w13: PackedWeights, w2: PackedWeig
                         stream=None, events=None, w13_bias: Optional[torch.Tensor] = None,
                         w2_bias: Optional[torch.Tensor] = None, activation: str = "silu",
                         swiglu=(1.702, 1.0, 7.0), w13_perm: Optional[torch.Tensor] = None,
-                        w2_inv_perm: Optional[torch.Tensor] = None) -> torch.Tensor:
+                        w2_inv_perm: Optional[torch.Tensor] = None, atomic_reduce: bool = False) -> torch.Tensor:
     """The fused layer on prepacked weights (``wna16_fused_moe_prepacked``; with
     model-variant options, ``wna16_fused_moe_prepacked_ex``)."""
     _check(hidden, "hidden", (torch.float16, torch.bfloat16))
@@ -562,7 +567,7 @@ def fused_moe_prepacked(hidden: torch.Tensor, w13: PackedWeights, w2: PackedWeig
     args = (_ptr(hidden), _DTYPE[hidden.dtype], M, H, I, E, topk, _ptr(w13.data), _ptr(w2.data),
             int(w13.has_zeros), _DTYPE[w13.scale_dtype], w13.bits, w13.group_size, _ptr(topk_ids),
             _ptr(topk_weights), _ptr(out), _ptr(workspace), workspace.numel(), block, split_k, _stream(stream), arr)
-    opt = _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu, w13_perm, w2_inv_perm)
+    opt = _options(hidden, E, I, H, w13_bias, w2_bias, activation, swiglu, w13_perm, w2_inv_perm, atomic_reduce)
     if opt is not None:
         st = load().wna16_fused_moe_prepacked_ex(*args, ctypes.byref(opt))
     else:

@@ -214,7 +214,8 @@ __global__ void __launch_bounds__(256)
     moe_gather_kernel(const uint4* __restrict__ hidden, const int32_t* __restrict__ ids,
                       const int32_t* __restrict__ slot_of_pair, int P, int topk, int E, int h8, int permute,
                       uint4* __restrict__ x_sorted, float* __restrict__ xs, int cap, float* __restrict__ zero0,
-                      int zero_n0, float* __restrict__ zero1, int zero_n1, float* __restrict__ zero2, int zero_n2) {
+                      int zero_n0, float* __restrict__ zero1, int zero_n1, float* __restrict__ zero2, int zero_n2,
+                      float* __restrict__ zero3, int zero_n3) {
   grid_dep_wait();
   grid_dep_launch();
   const int chunks = h8 / 8;
@@ -257,6 +258,7 @@ __global__ void __launch_bounds__(256)
   for (long long i = first; i < zero_n0; i += stride) zero0[i] = 0.f;
   for (long long i = first; i < zero_n1; i += stride) zero1[i] = 0.f;
   for (long long i = first; i < zero_n2; i += stride) zero2[i] = 0.f;
+  for (long long i = first; i < zero_n3; i += stride) zero3[i] = 0.f;
 }
 
 // Act-order gate/up weights: routed row p's expert e reads its hidden row in
@@ -308,7 +310,7 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
 template <typename T>
 __global__ void __launch_bounds__(256)
     moe_combine_kernel(const float* __restrict__ slab, const int32_t* __restrict__ ids, int M, int H,
-                       int topk, int E, int split, T* __restrict__ out) {
+                       int topk, int E, int split, int summed, T* __restrict__ out) {
   grid_dep_wait();
   const int h4 = H / 4;
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -317,7 +319,9 @@ __global__ void __launch_bounds__(256)
   const int h = static_cast<int>(idx % h4) * 4;
   const long long P = static_cast<long long>(M) * topk;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < topk; ++j) {
+  // summed: the down GEMM already added the slots and splits into [M, H]
+  if (summed) acc = *reinterpret_cast<const float4*>(slab + static_cast<long long>(t) * H + h);
+  for (int j = 0; j < (summed ? 0 : topk); ++j) {
     const int e = ids[t * topk + j];
     if (e < 0 || e >= E) continue;  // dropped pair
     for (int s = 0; s < split; ++s) {
@@ -372,10 +376,11 @@ cudaError_t launch_route_align(const void* logits, int logits_dtype, int M, int 
 cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
                           int topk, int E, int H, int permute, int act_dtype, int max_ctas, void* x_sorted,
                           float* xs, int cap, float* zero_ptr0, int zero_n0, float* zero_ptr1, int zero_n1,
-                          float* zero_ptr2, int zero_n2, cudaStream_t stream, bool pdl) {
+                          float* zero_ptr2, int zero_n2, float* zero_ptr3, int zero_n3, cudaStream_t stream,
+                          bool pdl) {
   const int h8 = H / 8;
   long long n = static_cast<long long>(P) * (h8 / 8);
-  n = std::max<long long>(n, std::max({zero_n0, zero_n1, zero_n2}));
+  n = std::max<long long>(n, std::max({zero_n0, zero_n1, zero_n2, zero_n3}));
   const int threads = 256;
   const long long want = (n + threads - 1) / threads;
   const unsigned blocks = static_cast<unsigned>(want < max_ctas ? want : max_ctas);
@@ -383,7 +388,7 @@ cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t*
   auto* fn = act_dtype == 0 ? moe_gather_kernel<0> : moe_gather_kernel<1>;
   return launch_kernel(fn, dim3(blocks), dim3(threads), 0, stream, pdl, static_cast<const uint4*>(hidden), ids,
                        slot_of_pair, P, topk, E, h8, permute, static_cast<uint4*>(x_sorted), xs, cap, zero_ptr0,
-                       zero_n0, zero_ptr1, zero_n1, zero_ptr2, zero_n2);
+                       zero_n0, zero_ptr1, zero_n1, zero_ptr2, zero_n2, zero_ptr3, zero_n3);
 }
 
 cudaError_t launch_gather_perm(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair,
@@ -400,15 +405,15 @@ cudaError_t launch_gather_perm(const void* hidden, const int32_t* ids, const int
 }
 
 cudaError_t launch_combine(const float* slab, const int32_t* ids, int M, int H, int topk, int E,
-                           int split, int act_dtype, void* out, cudaStream_t stream, bool pdl) {
+                           int split, int summed, int act_dtype, void* out, cudaStream_t stream, bool pdl) {
   const long long n = static_cast<long long>(M) * (H / 4);
   const int threads = 256;
   const unsigned blocks = static_cast<unsigned>((n + threads - 1) / threads);
   if (act_dtype == 0)
     return launch_kernel(moe_combine_kernel<__half>, dim3(blocks), dim3(threads), 0, stream, pdl, slab, ids, M, H,
-                         topk, E, split, static_cast<__half*>(out));
+                         topk, E, split, summed, static_cast<__half*>(out));
   return launch_kernel(moe_combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, stream, pdl, slab, ids, M,
-                       H, topk, E, split, static_cast<__nv_bfloat16*>(out));
+                       H, topk, E, split, summed, static_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace wna16

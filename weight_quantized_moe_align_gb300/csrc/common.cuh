@@ -107,6 +107,8 @@ struct GemmArgs {
   float glu_alpha, glu_beta, glu_limit;
   const int32_t* act_pos;      // gate/up GEMM, act-order down weights: [E, I] column of feature f in the act cache
   int pdl;                     // launched as a programmatic dependent of the previous kernel
+  float* atomic_out;           // down GEMM: [M, N] fp32 sum over slots and K splits by atomicAdd
+                               // (null: the ordered slab)
 };
 
 // One weight stage in shared memory: packed codes of 128 rows x 128 K, then up

@@ -636,8 +636,12 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         for (int j = 0; j < NT; ++j) {
           const int pid = __shfl_sync(0xFFFFFFFFu, my_pid, j);
           const float tw = __shfl_sync(0xFFFFFFFFu, my_w, j);
-          if (pid >= 0 && pid < a.P && hr < a.N)
-            slab[slab_index(w.sp, a.P, pid, a.N, hr)] = acc[j] * tw;
+          if (pid >= 0 && pid < a.P && hr < a.N) {
+            if (VAR && a.atomic_out)  // unordered fp32 sum over the token's slots and the K splits
+              atomicAdd(a.atomic_out + static_cast<size_t>(pid / a.topk) * a.N + hr, acc[j] * tw);
+            else
+              slab[slab_index(w.sp, a.P, pid, a.N, hr)] = acc[j] * tw;
+          }
         }
       }
     }

@@ -268,8 +268,12 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
       for (int j = 0; j < 16; ++j) {
         const int pid = __shfl_sync(0xFFFFFFFFu, my_pid, j);
         const float tw = __shfl_sync(0xFFFFFFFFu, my_w, j);
-        if (pid >= 0 && pid < a.P && h < a.N)
-          slab[slab_index(w.sp, a.P, pid, a.N, h)] = __uint_as_float(v[j]) * tw;
+        if (pid >= 0 && pid < a.P && h < a.N) {
+          if (EXT && a.atomic_out)  // unordered fp32 sum over the token's slots and the K splits
+            atomicAdd(a.atomic_out + static_cast<size_t>(pid / a.topk) * a.N + h, __uint_as_float(v[j]) * tw);
+          else
+            slab[slab_index(w.sp, a.P, pid, a.N, h)] = __uint_as_float(v[j]) * tw;
+        }
       }
     }
   }

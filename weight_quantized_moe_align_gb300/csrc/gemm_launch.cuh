@@ -38,11 +38,13 @@ cudaError_t launch_route_align(const void* logits, int logits_dtype, int M, int 
 // Expert-sorted copy of the hidden rows; with `xs` also the deferred-scale
 // token sums [H/128 stages][4 parts][cap]. It also zeroes the `zero_n` 32-bit
 // words at each `zero_ptr` (token-sum parts of a stage half with no K
-// elements, the gate/up GEMM's split arrival counters).
+// elements, the gate/up GEMM's split arrival counters, the down GEMM's atomic
+// accumulator).
 cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair, int P,
                           int topk, int E, int H, int permute, int act_dtype, int max_ctas, void* x_sorted,
                           float* xs, int cap, float* zero_ptr0, int zero_n0, float* zero_ptr1, int zero_n1,
-                          float* zero_ptr2, int zero_n2, cudaStream_t stream, bool pdl);
+                          float* zero_ptr2, int zero_n2, float* zero_ptr3, int zero_n3, cudaStream_t stream,
+                          bool pdl);
 // the gather for act-order gate/up weights: x_sorted rows in each expert's K order kperm [E, H]
 cudaError_t launch_gather_perm(const void* hidden, const int32_t* ids, const int32_t* slot_of_pair,
                                const int32_t* kperm, int P, int topk, int E, int H, int permute, int max_ctas,
@@ -51,7 +53,8 @@ cudaError_t launch_gather_perm(const void* hidden, const int32_t* ids, const int
 wna16_status routing_check(const void* logits, wna16_dtype logits_dtype, int64_t M, int E, int topk,
                            wna16_scoring scoring, int n_groups, int topk_groups, const int32_t* topk_ids,
                            const float* topk_weights);
+// summed != 0: `slab` is the down GEMM's [M, H] fp32 atomic accumulator (round only)
 cudaError_t launch_combine(const float* slab, const int32_t* ids, int M, int H, int topk, int E,
-                           int split, int act_dtype, void* out, cudaStream_t stream, bool pdl);
+                           int split, int summed, int act_dtype, void* out, cudaStream_t stream, bool pdl);
 
 }  // namespace wna16

@@ -40,7 +40,7 @@ cudaError_t launch_gemm_w4(int act, int scl, int gemm, int lean, dim3 grid, size
                             cudaStream_t stream, const CUtensorMap& q, const CUtensorMap& s,
                             const CUtensorMap& z, const CUtensorMap& b, const GemmArgs& a) {
   // EXT: prepacked weights, biases, clamped SwiGLU or act-order (not built for the lean layout)
-  const bool ext = a.wpack || a.bias || a.glu || a.act_pos;
+  const bool ext = a.wpack || a.bias || a.glu || a.act_pos || a.atomic_out;
   if (lean) {
     if (ext) return cudaErrorInvalidValue;
     if (gemm == 1) return by_dtype<1, 1, 0>(act, scl, grid, smem, stream, q, s, z, b, a);

@@ -41,7 +41,7 @@ cudaError_t launch_gemm_w8(int act, int scl, int gemm, int lean, dim3 grid, size
                             const CUtensorMap& z, const CUtensorMap& b, const GemmArgs& a) {
   if (lean) return cudaErrorInvalidValue;  // the lean layout is only built for 4-bit weights
   // EXT: prepacked weights, biases, clamped SwiGLU or act-order
-  if (a.wpack || a.bias || a.glu || a.act_pos)
+  if (a.wpack || a.bias || a.glu || a.act_pos || a.atomic_out)
     return gemm == 1 ? by_dtype<1, 0, 1>(act, scl, grid, smem, stream, q, s, z, b, a)
                      : by_dtype<2, 0, 1>(act, scl, grid, smem, stream, q, s, z, b, a);
   if (gemm == 1) return by_dtype<1, 0, 0>(act, scl, grid, smem, stream, q, s, z, b, a);

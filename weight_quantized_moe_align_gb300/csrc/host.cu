@@ -144,6 +144,8 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
       return WNA16_ERR_INVALID_ARG;
   }
   if (scale_dtype != WNA16_F16 && scale_dtype != WNA16_BF16) return WNA16_ERR_INVALID_ARG;
+  if (opt && opt->atomic_reduce && (opt->w13_perm || opt->w2_inv_perm)) return WNA16_ERR_INVALID_ARG;
+  if (M * H >= (int64_t(1) << 31)) return WNA16_ERR_UNSUPPORTED;
   Resolved r;
   const int sms = sm_count();
   const wna16_status st = resolve(M, H, I, E, topk, bits, group_size, block, split_k, sms, &r);
@@ -234,7 +236,8 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   } else if (!mark(1) || launch_gather(hidden, topk_ids, slot_of_pair, p.P, topk, E, static_cast<int>(H),
                                        bits == 4 ? 1 : 0, act_dtype, p.gather_ctas, x_sorted,
                                        p.defer ? ws_words + p.L.xs1 / 4 : nullptr, static_cast<int>(p.cap), zero1,
-                                       p.zero1_n, zero2, p.zero2_n, cnt1, p.cnt1_n, s, p.pdl) != cudaSuccess) {
+                                       p.zero1_n, zero2, p.zero2_n, cnt1, p.cnt1_n,
+                                       p.acc_n ? ws_words + p.acc_off : nullptr, p.acc_n, s, p.pdl) != cudaSuccess) {
     return WNA16_ERR_CUDA;
   }
 
@@ -252,7 +255,8 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   if (e2 != cudaSuccess) return WNA16_ERR_CUDA;
 
   if (!mark(4) || launch_combine(reinterpret_cast<const float*>(ws + p.L.slab), topk_ids, static_cast<int>(M),
-                                 static_cast<int>(H), topk, E, p.r.split, act_dtype, out, s, p.pdl) != cudaSuccess)
+                                 static_cast<int>(H), topk, E, p.r.split, p.atomic ? 1 : 0, act_dtype, out, s,
+                                 p.pdl) != cudaSuccess)
     return WNA16_ERR_CUDA;
   if (!mark(5)) return WNA16_ERR_CUDA;
   return WNA16_OK;

@@ -374,6 +374,13 @@ wna16_status plan_layer(wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I, 
     p.cnt1_off = p.L.cnt1 / 4;
     p.cnt1_n = static_cast<int>((I / kGateUpRows) * p.max_blocks * 4);
   }
+  // down GEMM reduced with fp32 atomics into an [M, H] accumulator at the
+  // slab's start (split * P * H >= M * H floats), zeroed by the gather
+  p.atomic = opt && opt->atomic_reduce;
+  if (p.atomic) {
+    p.acc_off = p.L.slab / 4;
+    p.acc_n = static_cast<int>(M * H);
+  }
   p.gather_ctas = sms * 8;
   p.pipe = pipe_for(bits, p.B);
 
@@ -447,6 +454,7 @@ wna16_status plan_layer(wna16_dtype act_dtype, int64_t M, int64_t H, int64_t I, 
   a2.G = p.r.G2;
   a2.kt_total = p.kt2;
   a2.split = p.r.split;
+  a2.atomic_out = p.atomic ? reinterpret_cast<float*>(ws + p.L.slab) : nullptr;
 
   const int64_t slots = static_cast<int64_t>(sms) * p.pipe.ctas_per_sm;
   const int64_t units1 = static_cast<int64_t>(p.max_blocks) * a1.n_tiles * a1.split;

@@ -67,7 +67,7 @@ struct LayerPlan {
   Pipe pipe;
   int P, B, max_blocks, kt1, kt2, split1, sms;
   int64_t cap;
-  bool defer, packed, zeros, act_order, pdl, routed;
+  bool defer, packed, zeros, act_order, pdl, routed, atomic;
   GemmArgs a1, a2;
   unsigned grid1, grid2;
   size_t smem1, smem2;
@@ -75,8 +75,8 @@ struct LayerPlan {
   GemmMaps m1, m2;                // unused (zeroed) for prepacked weights, except the token maps
   // zero fills done by the gather launch (token sums of empty stage halves,
   // split arrival counters), as offsets into the workspace in 4-byte words
-  size_t zero1_off, zero2_off, cnt1_off;
-  int zero1_n, zero2_n, cnt1_n;
+  size_t zero1_off, zero2_off, cnt1_off, acc_off;
+  int zero1_n, zero2_n, cnt1_n, acc_n;
   int gather_ctas;
 };
 
