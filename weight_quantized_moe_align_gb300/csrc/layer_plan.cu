@@ -43,30 +43,20 @@ int64_t expected_blocks(int64_t M, int topk, int E, int block) {
   return active * ((avg + block - 1) / block);
 }
 
-// K split of a GEMM launch. The persistent CTAs take the units in rounds, so
-// a launch lasts about ceil(units * s / slots) unit times, and a unit of split
-// s lasts kt/s stages plus a fixed cost at its boundary (accumulator handoff,
-// epilogue, the split's partial-sum exchange), taken as kUnitCost stages. The
-// split with the least such time wins (ties to fewer splits), at most 8 and
-// keeping >= 8 stages per split. One round of unsplit units that leaves half
-// the slots idle (two routed experts at decode) is where it pays.
-constexpr double kUnitCost = 4.0;
-
+// K split of a GEMM launch: only when the units do not fill the persistent CTA
+// slots, then as many splits as fit (at most 8, keeping >= 8 K stages per
+// split). Finer splits that merely even out the rounds were measured slower:
+// every unit boundary stalls the dequant chain (accumulator handoff, epilogue,
+// and for the gate/up GEMM the partial-sum exchange). On one GB300, splitting
+// the gate/up GEMM of an 8-expert layer at one token (448 units on 304 slots)
+// in two raised it from 38 to 49 us.
 int choose_split(int64_t units, int kt_total, int ctas_per_sm, int sms) {
   const int64_t slots = static_cast<int64_t>(sms) * ctas_per_sm;
-  if (units <= 0) return 1;
-  const int max_s = std::max(1, std::min(8, kt_total / 8));
-  int best = 1;
-  double best_t = 1e300;
-  for (int s = 1; s <= max_s; ++s) {
-    const double rounds = static_cast<double>((units * s + slots - 1) / slots);
-    const double t = rounds * (static_cast<double>(kt_total) / s + kUnitCost);
-    if (t < best_t - 1e-9) {
-      best_t = t;
-      best = s;
-    }
-  }
-  return best;
+  if (units >= slots) return 1;
+  int s = static_cast<int>(slots / std::max<int64_t>(units, 1));
+  s = std::min(s, 8);
+  s = std::min(s, std::max(1, kt_total / 8));
+  return std::max(s, 1);
 }
 
 // Gate/up (rows = 2I): codes [E*2 halves, I, K/pf] box {128/pf, 64, 2} (gate
