@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libwna16_moe.so")
-SOURCES = ["host.cu", "layer_plan.cu", "plan_check.cu", "align_combine.cu", "gemm_w4.cu", "gemm_w4_wide.cu", "gemm_w8.cu", "gemm_w8_wide.cu", "gemm_defer.cu", "gemm_defer_var.cu", "prepack.cu", "noalloc.cu", "routing.cu", "act_order.cu", "convert.cu", "selftest.cu"]
+SOURCES = ["host.cu", "layer_plan.cu", "plan_check.cu", "align_combine.cu", "gemm_w4.cu", "gemm_w8.cu", "gemm_defer.cu", "gemm_defer_var.cu", "prepack.cu", "noalloc.cu", "routing.cu", "act_order.cu", "convert.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

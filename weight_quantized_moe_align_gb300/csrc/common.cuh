@@ -13,13 +13,15 @@ namespace wna16 {
 //   0      TMA producer (packed weights, scales, zero points, token tile)
 //   1      tcgen05 MMA issuer, owner of the TMEM allocation
 //   2..5   epilogue (TMEM -> registers -> global); lane quarter = warp % 4
-//   6..    dequantizers, stage-parallel warpgroups of 4 warps (shared -> registers -> TMEM):
-//          two when two CTAs share an SM (token tiles up to 64: 256 TMEM
-//          columns, <= 112 KB of shared memory each), three in the one-CTA-per-SM
-//          layout of larger tiles (WIDE = 1), whose register file has room for them.
+//   6..13  dequantizers, two stage-parallel warpgroups (shared -> registers -> TMEM)
+// A lean layout (producer, MMA issuer, 4 dequant warps that also run the
+// epilogue) fits four CTAs per SM for int4 token tiles up to 32 (128 TMEM
+// columns, <= 56 KB of shared memory each): four MMA-issuing threads share the
+// tensor core. Other tiles up to 64 run two CTAs per SM of the full layout
+// (256 TMEM columns, <= 112 KB each); larger tiles take the whole SM.
+constexpr int kDequantWarps = 8;   // two warpgroups (LEAN = 0); LEAN = 1 uses one
 constexpr int kEpilogueWarps = 4;
-__host__ __device__ constexpr int dequant_groups(int wide) { return wide ? 3 : 2; }
-__host__ __device__ constexpr int gemm_threads(int wide) { return (2 + kEpilogueWarps + 4 * dequant_groups(wide)) * 32; }
+__host__ __device__ constexpr int gemm_threads(int lean) { return lean ? 6 * 32 : 14 * 32; }
 
 constexpr int kTileK = 128;      // K elements per pipeline stage
 constexpr int kChunkK = 64;      // K elements per 128-byte swizzle atom of the token tile

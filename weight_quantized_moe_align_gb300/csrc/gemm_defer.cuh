@@ -426,27 +426,18 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
       for (int i = (g - it) & 1; i < n; i += 2) {
         if (!warp_wait_all(&full[cs], cf, abort_flag, a.status)) { ok = false; break; }
         // the previous stage's MMAs done: A slot, correction rows and P_g free;
-        // its partial sum, scaled into the accumulators. With 16-token tiles the
-        // partial sum's TMEM load stays in flight while this stage's codes are
-        // unpacked and stored (it is awaited before the MMA warp is signalled,
-        // since the next MMA into P_g follows that signal); 32-token tiles
-        // (twice the registers) wait for it at once.
-        uint32_t pv[16];
+        // its partial sum, scaled into the accumulators
         if (pending) {
           if (!warp_wait_all(&pfull[g], pph, abort_flag, a.status)) { ok = false; break; }
           tc_fence_after();
           pph ^= 1u;
-          if constexpr (NT == 16) {
-            tmem_ld16(p_addr, pv);
-          } else {
 #pragma unroll
-            for (int c0 = 0; c0 < NT; c0 += 16) {
-              uint32_t v[16];
-              tmem_ld16(p_addr + c0, v);
-              tmem_ld_wait(v);
+          for (int c0 = 0; c0 < NT; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(p_addr + c0, v);
+            tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(pscale, __uint_as_float(v[j]), acc[c0 + j]);
-            }
+            for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(pscale, __uint_as_float(v[j]), acc[c0 + j]);
           }
         }
         const uint8_t* st = wring + cs * WST;
@@ -491,14 +482,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
           row[1 ^ (lane & 7)] = make_uint4(0u, 0u, 0u, 0u);  // K 8..15
           fence_proxy_async_smem();
         }
-        __syncwarp();  // reconverge before the warp-wide tcgen05 waits
-        if constexpr (NT == 16) {
-          if (pending) {
-            tmem_ld_wait(pv);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = fmaf(pscale, __uint_as_float(pv[j]), acc[j]);
-          }
-        }
+        __syncwarp();  // reconverge before the warp-wide tcgen05 wait
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -522,7 +506,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
           for (int c0 = 0; c0 < NT; c0 += 16) {
             uint32_t v[16];
             tmem_ld16(p_addr + c0, v);
-            tmem_ld_wait(v);
+            tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(pscale, __uint_as_float(v[j]), acc[c0 + j]);
           }
@@ -555,7 +539,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
       for (int c0 = 0; c0 < NT; c0 += 16) {
         uint32_t v[16];
         tmem_ld16(c_addr + c0, v);
-        tmem_ld_wait(v);
+        tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc[c0 + j] += __uint_as_float(v[j]);
       }

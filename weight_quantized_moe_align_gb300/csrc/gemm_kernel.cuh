@@ -232,7 +232,7 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
   for (int c0 = 0; c0 < ncols; c0 += 16) {
     uint32_t v[16];
     tmem_ld16(t_base + c0, v);
-    tmem_ld_wait(v);
+    tmem_ld_wait();
     if (has_bias) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + bias);
@@ -283,16 +283,16 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
   return true;
 }
 
-// WIDE = 0: 14 warps (producer, MMA issuer, 4 epilogue warps, two dequant
-// warpgroups), two CTAs per SM. WIDE = 1: 18 warps with three dequant
-// warpgroups, one CTA per SM (token tiles of 128 and 256).
+// LEAN = 0: 14 warps (producer, MMA issuer, 4 epilogue warps, two dequant
+// warpgroups), two CTAs per SM. LEAN = 1: 6 warps (producer, MMA issuer, one
+// dequant warpgroup that also runs the epilogue), four CTAs per SM, so four
+// MMA-issuing threads share the SM's tensor core (decode-sized token tiles).
 //
 // EXT = 1: the instantiations that also serve prepacked weights, biases, the
-// clamped SwiGLU, act-order and the atomic down reduction; EXT = 0 carries
-// none of that code (the register-bound dequant loop was measurably slower
-// with it).
-template <int BITS, int ACT, int SCL, int GEMM, int WIDE, int EXT>
-__global__ void __launch_bounds__(gemm_threads(WIDE), WIDE ? 1 : 2)
+// clamped SwiGLU and act-order; EXT = 0 carries none of that code (the
+// register-bound dequant loop was measurably slower with it).
+template <int BITS, int ACT, int SCL, int GEMM, int LEAN, int EXT>
+__global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_s,
                     const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_b,
                     const GemmArgs a) {
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(gemm_threads(WIDE), WIDE ? 1 : 2)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < NA; ++i) mbar_init(&afull[i], 4);  // the 4 warps of one warpgroup per stage
+    for (int i = 0; i < NA; ++i) mbar_init(&afull[i], kDequantWarps / 2);  // one warpgroup per stage
     for (int i = 0; i < NACC; ++i) {
       mbar_init(&accfull[i], 1);
       mbar_init(&accempty[i], kEpilogueWarps);
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(gemm_threads(WIDE), WIDE ? 1 : 2)
       __syncwarp();
       wait_bar_drain(drain, 0);
     }
-  } else if (warp < 2 + kEpilogueWarps) {
+  } else if (!LEAN && warp < 2 + kEpilogueWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int uc = 0;
@@ -479,13 +479,14 @@ __global__ void __launch_bounds__(gemm_threads(WIDE), WIDE ? 1 : 2)
     }
   } else {
     // ------------------------------------------------------------ dequantizers
-    // NG stage-parallel warpgroups: warpgroup g dequantizes the stages whose
-    // running index is congruent to g mod NG, so NG stages are in flight. One
-    // full 128-element K row per thread (thread = TMEM lane = weight row).
+    // LEAN = 0: two warpgroups, stage-parallel: warpgroup g dequantizes the
+    // stages whose running index is congruent to g mod 2, so two stages are in
+    // flight. LEAN = 1: one warpgroup takes every stage. One full 128-element K
+    // row per thread (thread = TMEM lane = weight row).
     // A slot it % NA is free once the MMAs of stage it - NA completed, which is
     // the completion of that stage's `empty` phase.
     const int q = warp & 3;
-    const int grp = (warp - 2 - kEpilogueWarps) >> 2;
+    const int grp = LEAN ? 0 : (warp - 2 - kEpilogueWarps) >> 2;
     // Weight row (in the stage's smem tile) of this thread's TMEM lane. Gate/up:
     // lanes 0-15 of quarter q take gate rows 16q.., lanes 16-31 the up rows of
     // the same features, so the epilogue finds gate and up in one warp.
@@ -500,18 +501,19 @@ __global__ void __launch_bounds__(gemm_threads(WIDE), WIDE ? 1 : 2)
     }
     const uint32_t t_lane = (q * 32) << 16;
     const int z_off = (EXT && a.wpack) ? W_BYTES + SG * 256 : Z_OFF;  // zero points: right after the scales in an image
-    // This group's stages are the running stage indices gi = grp, grp + NG,
-    // ... across units. Tracked incrementally: the ring slot cs and phase cf of
-    // stage gi, its A slot cslot, and the ring slot cps and phase cp of stage
-    // gi - NA, whose completed MMAs free that A slot (floor division, so the
-    // tracking stays consistent through gi < NA).
-    constexpr int step = dequant_groups(WIDE);  // may exceed the ring: wrap with a loop
+    // This group's stages are the running stage indices gi = grp, grp + step,
+    // ... across units (step 2, or 1 for LEAN). Tracked incrementally: the ring
+    // slot cs and phase cf of stage gi, its A slot cslot, and the ring slot cps
+    // and phase cp of stage gi - NA, whose completed MMAs free that A slot
+    // (floor division, so the tracking stays consistent through gi < NA).
+    constexpr int step = LEAN ? 1 : 2;  // the ring has NS >= 2 stages, so one wrap suffices for cs, cps
     const int pfirst = grp - NA;
     int cs = grp % NS, cslot = grp % NA, gi = grp;
     int cps = ((pfirst % NS) + NS) % NS;
     uint32_t cf = (grp / NS) & 1u;
     uint32_t cp = static_cast<uint32_t>((pfirst >= 0 ? pfirst / NS : (pfirst - NS + 1) / NS) & 1);
     int it = 0;  // running index of the current unit's first stage
+    int uc = 0;  // units finished (epilogue count, LEAN)
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit w = decode_unit(u, nb, a);
       const int n = w.kt1 - w.kt0;
@@ -561,12 +563,12 @@ __global__ void __launch_bounds__(gemm_threads(WIDE), WIDE ? 1 : 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[cslot]);
         cs += step;
-        while (cs >= NS) {
+        if (cs >= NS) {
           cs -= NS;
           cf ^= 1u;
         }
         cps += step;
-        while (cps >= NS) {
+        if (cps >= NS) {
           cps -= NS;
           cp ^= 1u;
         }
@@ -575,6 +577,13 @@ __global__ void __launch_bounds__(gemm_threads(WIDE), WIDE ? 1 : 2)
       }
       it += n;
       if (!ok) break;
+      if (LEAN) {
+        // this warpgroup also runs the epilogue, right after the unit's last stage
+        if (!epilogue_unit<BITS, ACT, GEMM, EXT>(a, w, tmem, uc % NACC, (uc / NACC) & 1, accfull, accempty, abort_flag, q,
+                                      lane))
+          break;
+        ++uc;
+      }
     }
   }
 

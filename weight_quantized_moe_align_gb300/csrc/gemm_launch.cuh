@@ -6,20 +6,13 @@
 
 namespace wna16 {
 
-// gemm: 1 = gate/up + silu*up epilogue, 2 = down + top-k weight epilogue;
-// wide: the one-CTA-per-SM layout with three dequant warpgroups.
-cudaError_t launch_gemm_w4(int act, int scl, int gemm, int wide, dim3 grid, size_t smem, cudaStream_t stream,
+// gemm: 1 = gate/up + silu*up epilogue, 2 = down + top-k weight epilogue.
+cudaError_t launch_gemm_w4(int act, int scl, int gemm, int lean, dim3 grid, size_t smem, cudaStream_t stream,
                            const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                            const CUtensorMap& b, const GemmArgs& a);
-cudaError_t launch_gemm_w8(int act, int scl, int gemm, int wide, dim3 grid, size_t smem, cudaStream_t stream,
+cudaError_t launch_gemm_w8(int act, int scl, int gemm, int lean, dim3 grid, size_t smem, cudaStream_t stream,
                            const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
                            const CUtensorMap& b, const GemmArgs& a);
-cudaError_t launch_gemm_w4_wide(int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
-                                const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
-                                const CUtensorMap& b, const GemmArgs& a);
-cudaError_t launch_gemm_w8_wide(int act, int scl, int gemm, dim3 grid, size_t smem, cudaStream_t stream,
-                                const CUtensorMap& q, const CUtensorMap& s, const CUtensorMap& z,
-                                const CUtensorMap& b, const GemmArgs& a);
 
 // Deferred-scale GEMM for 16-token tiles; `x` maps the per-stage token sums.
 bool defer_supported(int bits, int act);

@@ -74,10 +74,10 @@ bool encode_maps(EncodedMaps* e, const GemmMaps& g, bool weights) {
   return !g.has_x || encode_map(&e->x, g.x);
 }
 
-cudaError_t launch_gemm(int bits, int act, int scl, int gemm, int wide, dim3 grid, size_t smem, cudaStream_t st,
+cudaError_t launch_gemm(int bits, int act, int scl, int gemm, int lean, dim3 grid, size_t smem, cudaStream_t st,
                         const EncodedMaps& m, const GemmArgs& a) {
-  return bits == 4 ? launch_gemm_w4(act, scl, gemm, wide, grid, smem, st, m.q, m.s, m.z, m.b, a)
-                   : launch_gemm_w8(act, scl, gemm, wide, grid, smem, st, m.q, m.s, m.z, m.b, a);
+  return bits == 4 ? launch_gemm_w4(act, scl, gemm, lean, grid, smem, st, m.q, m.s, m.z, m.b, a)
+                   : launch_gemm_w8(act, scl, gemm, lean, grid, smem, st, m.q, m.s, m.z, m.b, a);
 }
 
 }  // namespace
@@ -245,13 +245,13 @@ wna16_status run_layer(const void* hidden, wna16_dtype act_dtype, int64_t M, int
   const cudaError_t e1 =
       p.defer ? launch_gemm_defer(bits, act_dtype, scale_dtype, 1, dim3(p.grid1), p.smem1, s, m1.q, m1.s, m1.z, m1.b,
                                   m1.x, p.a1)
-              : launch_gemm(bits, act_dtype, scale_dtype, 1, p.pipe.wide, dim3(p.grid1), p.smem1, s, m1, p.a1);
+              : launch_gemm(bits, act_dtype, scale_dtype, 1, p.pipe.lean, dim3(p.grid1), p.smem1, s, m1, p.a1);
   if (e1 != cudaSuccess) return WNA16_ERR_CUDA;
   if (!mark(3)) return WNA16_ERR_CUDA;
   const cudaError_t e2 =
       p.defer ? launch_gemm_defer(bits, act_dtype, scale_dtype, 2, dim3(p.grid2), p.smem2, s, m2.q, m2.s, m2.z, m2.b,
                                   m2.x, p.a2)
-              : launch_gemm(bits, act_dtype, scale_dtype, 2, p.pipe.wide, dim3(p.grid2), p.smem2, s, m2, p.a2);
+              : launch_gemm(bits, act_dtype, scale_dtype, 2, p.pipe.lean, dim3(p.grid2), p.smem2, s, m2, p.a2);
   if (e2 != cudaSuccess) return WNA16_ERR_CUDA;
 
   if (!mark(4) || launch_combine(reinterpret_cast<const float*>(ws + p.L.slab), topk_ids, static_cast<int>(M),

@@ -16,6 +16,7 @@ namespace {
 
 constexpr int kMaxSmem = 232448;         // opt-in dynamic shared memory per CTA on sm_103a
 constexpr int kHalfSmem = 112 * 1024;    // two CTAs per SM
+constexpr int kQuarterSmem = 55 * 1024;  // four CTAs per SM
 constexpr int kMinSmem = 120 * 1024;     // a whole-SM CTA (512 TMEM columns) runs alone on its SM
 
 bool is_pow2(long long v) { return v > 0 && (v & (v - 1)) == 0; }
@@ -197,18 +198,23 @@ int choose_block_impl(int64_t M, int topk, int E) {
 }
 
 // Pipeline shape of one GEMM launch for a token tile of `block`.
-//  * tiles up to 64: two CTAs per SM (256 TMEM columns, <= 112 KB of shared
-//    memory each, two dequant warpgroups);
-//  * larger tiles: one CTA per SM (512 TMEM columns, three dequant
-//    warpgroups: the wide layout).
+//  * lean layout (when selected): four CTAs per SM (128 TMEM columns: one
+//    accumulator and one A slot; <= 55 KB of shared memory each), four
+//    MMA-issuing threads sharing the tensor core.
+//  * tiles up to 64: two CTAs per SM of the full layout (256 TMEM columns,
+//    <= 112 KB of shared memory).
+//  * larger tiles: one CTA per SM.
 Pipe pipe_for(int bits, int block) {
   Pipe p;
-  const bool half_sm = block <= 64;
-  p.wide = half_sm ? 0 : 1;
-  p.ctas_per_sm = half_sm ? 2 : 1;
-  p.tmem_cols = half_sm ? 256 : 512;
-  const int smem_cap = half_sm ? kHalfSmem : kMaxSmem;
-  p.acc = (2 * block + 2 * kASlotCols <= static_cast<int>(p.tmem_cols)) ? 2 : 1;
+  // The lean layout (LEAN = 1) is built and selectable here; measured on
+  // Mixtral-8x7B decode it was slower than two full-layout CTAs per SM (its
+  // single A slot serialises dequant and MMA inside each CTA), so it is off.
+  p.lean = 0;
+  const bool half_sm = !p.lean && block <= 64;
+  p.ctas_per_sm = p.lean ? 4 : (half_sm ? 2 : 1);
+  p.tmem_cols = p.lean ? 128 : (half_sm ? 256 : 512);
+  const int smem_cap = p.lean ? kQuarterSmem : (half_sm ? kHalfSmem : kMaxSmem);
+  p.acc = p.lean ? 1 : ((2 * block + 2 * kASlotCols <= static_cast<int>(p.tmem_cols)) ? 2 : 1);
   p.stages = kMaxStages;
   while (p.stages > 2 && gemm_smem_bytes(bits, block, p.stages) > smem_cap) --p.stages;
   p.aslots = std::min({kMaxASlots, (static_cast<int>(p.tmem_cols) - p.acc * block) / kASlotCols, p.stages - 1});

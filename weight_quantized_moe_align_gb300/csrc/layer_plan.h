@@ -20,7 +20,7 @@ int choose_block_impl(int64_t M, int topk, int E);
 
 // Pipeline shape of one general-kernel launch for a token tile of `block`.
 struct Pipe {
-  int stages, aslots, acc, ctas_per_sm, wide;
+  int stages, aslots, acc, ctas_per_sm, lean;
   uint32_t tmem_cols;
   size_t smem;
 };
