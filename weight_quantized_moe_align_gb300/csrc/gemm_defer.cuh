@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
           for (int c0 = 0; c0 < NT; c0 += 16) {
             uint32_t v[16];
             tmem_ld16(p_addr + c0, v);
-            tmem_ld_wait();
+            tmem_ld_wait(v);
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(pscale, __uint_as_float(v[j]), acc[c0 + j]);
           }
@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
           for (int c0 = 0; c0 < NT; c0 += 16) {
             uint32_t v[16];
             tmem_ld16(p_addr + c0, v);
-            tmem_ld_wait();
+            tmem_ld_wait(v);
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(pscale, __uint_as_float(v[j]), acc[c0 + j]);
           }
@@ -539,7 +539,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
       for (int c0 = 0; c0 < NT; c0 += 16) {
         uint32_t v[16];
         tmem_ld16(c_addr + c0, v);
-        tmem_ld_wait();
+        tmem_ld_wait(v);
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc[c0 + j] += __uint_as_float(v[j]);
       }

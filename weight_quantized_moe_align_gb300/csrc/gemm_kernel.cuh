@@ -232,7 +232,7 @@ __device__ __forceinline__ bool epilogue_unit(const GemmArgs& a, const Unit& w, 
   for (int c0 = 0; c0 < ncols; c0 += 16) {
     uint32_t v[16];
     tmem_ld16(t_base + c0, v);
-    tmem_ld_wait();
+    tmem_ld_wait(v);
     if (has_bias) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + bias);
