@@ -650,6 +650,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();  // the drain wait above is per lane: converge before the .aligned dealloc
     tc_fence_after();
     tmem_dealloc(tmem, kDeferTmemCols);
   }

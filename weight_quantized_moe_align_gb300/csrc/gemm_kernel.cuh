@@ -590,6 +590,7 @@ __global__ void __launch_bounds__(gemm_threads(LEAN), LEAN ? 4 : 2)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();  // the drain wait above is per lane: converge before the .aligned dealloc
     tc_fence_after();
     tmem_dealloc(tmem, a.tmem_cols);
   }

@@ -88,15 +88,16 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-// wait_bar for a whole converged warp. Every lane polls the same barrier in the
-// same instructions; after a slow wait the vote keeps the warp converged and
-// the result uniform, so the caller can go on with warp-uniform code
-// (elect_one below).
+// wait_bar for a whole converged warp; the warp leaves converged with a
+// uniform result, so the caller can go on with warp-synchronous code
+// (elect_one, the .sync.aligned tcgen05 instructions). try_wait may suspend
+// each lane on its own and return as the phase completes, so the lanes of one
+// warp can see different results of the same probe: the fast path is taken
+// only when every lane saw the phase complete (a vote), never by some lanes
+// alone, which would leave the others in the slow path's vote without them.
 __device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               int* status) {
-  // The first probe is one warp-wide instruction reading one barrier word, so
-  // its result is the same in every lane; only the slow path needs the vote.
-  if (mbar_try_wait(bar, parity)) return true;
+  if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
   return __all_sync(0xFFFFFFFFu, wait_bar(bar, parity, abort_flag, status));
 }
 

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(96, 1) wait_timeout_kernel(int32_t* status, in
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_holder, 32);
   }
