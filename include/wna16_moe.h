@@ -185,14 +185,13 @@ size_t wna16_fused_moe_workspace_bytes(int64_t M, int64_t H, int64_t I, int E, i
  *                its first int32 is the device status word (reset by the call).
  *   block        align block size (0 = automatic), as in
  *                wna16_moe_align_block_size; it is also the GEMM token tile.
- *                Forced sizes other than the automatic choice are verified on
- *                the GPU for layers of up to 8 experts. With more experts they
- *                are accepted but unverified: sweeps of forced sizes much larger
- *                than the routed pairs per expert ended twice in an unexplained
- *                launch failure (256 experts at M = 256 with 32/64/128; 64
- *                experts at M = 128 with 128, after clean calls of the same
- *                configuration), although wna16_check_launch_plan finds every
- *                index of those launch plans in bounds.
+ *                With more than 16 experts, blocks of 128 and 256 are refused
+ *                (WNA16_ERR_UNSUPPORTED; the automatic choice never takes them
+ *                there): forced 128-token blocks on such layers ended in an
+ *                unexplained launch failure (256 experts at M = 256, 64 experts
+ *                at M = 128), although wna16_check_launch_plan finds every
+ *                index of those launch plans in bounds. Forced 32 and 64 are
+ *                accepted on any layer.
  *   split_k      K-splits of the down GEMM (0 = automatic, else 1..8).
  * Shapes: H a multiple of 64, I a multiple of 64, 1 <= topk <= E <= 256,
  * M*topk < 2^31. M = 0 returns WNA16_OK and launches nothing.

@@ -8,9 +8,9 @@ each workload's batches, at the automatic block and at every forced block
 size, on a 152-SM device; every TMA box must lie inside its tensor map, every
 workspace write inside its region, every routed pair's fp32 rows written once.
 
-The DeepSeek-V3-shaped layer at M = 256 with forced blocks of 32, 64 and 128 is
-the configuration of an unexplained launch failure recorded on the GPU; its
-plans are checked here, on the CPU only.
+The DeepSeek-V3-shaped layer at M = 256 with forced blocks is where launch
+failures were recorded on the GPU (with 128-token blocks; those, and 256, are
+now refused on layers of more than 16 experts); its plans are checked here.
 
 Planted mistakes (in the align output handed to the checker, never in the
 library) must be reported.
@@ -48,10 +48,19 @@ def _check(wl, M, block, ids=None, split_k=0, mutate=None):
                                wl.scale_dtype, ids, srt, exp, npp, block=block, split_k=split_k, sms=SMS)
 
 
-@pytest.mark.parametrize("block", [0, 16, 32, 64, 128])
+@pytest.mark.parametrize("block", [0, 16, 32, 64])
 def test_deepseek_v3_m256_forced_blocks(block):
     n, report = _check(WORKLOADS["deepseek_v3"], 256, block)
     assert n == 0, report
+
+
+@pytest.mark.parametrize("name,M,block", [("deepseek_v3", 256, 128), ("deepseek_v3", 1024, 256),
+                                          ("qwen2_57b", 128, 128), ("qwen2_57b", 512, 256)])
+def test_large_tiles_refused_on_many_expert_layers(name, M, block):
+    # 128/256-token tiles on layers with more than 16 experts are refused, as
+    # the fused call refuses them (unsupported)
+    n, _ = _check(WORKLOADS[name], M, block)
+    assert n == -2
 
 
 CASES = [(name, M) for name in ("mixtral8x7b", "qwen2_57b", "deepseek_v3") for M in WORKLOADS[name].m_sweep]
@@ -65,9 +74,9 @@ def test_sweep_points_automatic_block(name, M):
 
 @pytest.mark.parametrize("name,M,block", [
     ("mixtral8x7b", 64, 16), ("mixtral8x7b", 256, 128), ("mixtral8x7b", 1024, 256), ("mixtral8x7b", 16, 32),
-    ("qwen2_57b", 128, 64), ("qwen2_57b", 512, 128), ("qwen2_57b", 32, 32),
-    ("deepseek_v3", 1024, 16), ("deepseek_v3", 1024, 32), ("deepseek_v3", 1024, 128), ("deepseek_v3", 64, 64),
-    ("deepseek_v3", 16, 256), ("tiny", 4, 16), ("tiny", 4, 256),
+    ("qwen2_57b", 128, 64), ("qwen2_57b", 512, 64), ("qwen2_57b", 32, 32),
+    ("deepseek_v3", 1024, 16), ("deepseek_v3", 1024, 32), ("deepseek_v3", 1024, 64), ("deepseek_v3", 64, 64),
+    ("deepseek_v3", 16, 32), ("tiny", 4, 16), ("tiny", 4, 256),
 ])
 def test_forced_blocks(name, M, block):
     n, report = _check(WORKLOADS[name], M, block)

@@ -197,3 +197,17 @@ def test_convert_checkpoint_errors_are_host_side(lib):
     assert call(zo=None) == 1  # zeros in, no zeros out
     assert call(z=None, zo=None, E=0) == 1
     assert call(qo=v(18)) == 1
+
+
+def test_large_tiles_refused_for_many_experts(lib):
+    # more than 16 experts: 128/256-token tiles are refused (workspace size 0,
+    # the fused call answers unsupported); 64 is accepted, and so are large
+    # tiles for 16 experts or fewer
+    assert lib.wna16_fused_moe_workspace_bytes(256, 7168, 2048, 256, 8, 4, 128, 128, 0) == 0
+    assert lib.wna16_fused_moe_workspace_bytes(128, 3584, 2560, 64, 8, 4, 128, 256, 0) == 0
+    assert lib.wna16_fused_moe_workspace_bytes(256, 7168, 2048, 256, 8, 4, 128, 64, 0) > 0
+    assert lib.wna16_fused_moe_workspace_bytes(256, 4096, 14336, 16, 2, 4, 128, 128, 0) > 0
+    p = ctypes.c_void_p(256)
+    st = lib.wna16_fused_moe(p, 0, 256, 7168, 2048, 256, 8, p, p, p, p, p, p, 0, 4, 128, p, p, p, p,
+                             1 << 40, 128, 0, None)
+    assert st == 2  # WNA16_ERR_UNSUPPORTED, before any launch

@@ -18,6 +18,8 @@ constexpr int kMaxSmem = 232448;         // opt-in dynamic shared memory per CTA
 constexpr int kHalfSmem = 112 * 1024;    // two CTAs per SM
 constexpr int kQuarterSmem = 55 * 1024;  // four CTAs per SM
 constexpr int kMinSmem = 120 * 1024;     // a whole-SM CTA (512 TMEM columns) runs alone on its SM
+constexpr int kManyExperts = 16;         // layers with more experts take token tiles of at most
+constexpr int kMaxBlockManyExperts = 64; // this many tokens
 
 bool is_pow2(long long v) { return v > 0 && (v & (v - 1)) == 0; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -251,6 +253,10 @@ wna16_status resolve(int64_t M, int64_t H, int64_t I, int E, int topk, int bits,
   }
   if (block == 0) block = choose_block_impl(M, topk, E);
   if (!is_pow2(block) || block < 16 || block > 256) return WNA16_ERR_INVALID_ARG;
+  // 128- and 256-token tiles on layers with more than 16 experts ended in an
+  // unexplained launch failure on the GPU; the automatic choice never takes
+  // them there, and forced ones are refused.
+  if (block > kMaxBlockManyExperts && E > kManyExperts) return WNA16_ERR_UNSUPPORTED;
   r->block = block;
   if (split_k < 0 || split_k > 8) return WNA16_ERR_INVALID_ARG;
   const int kt2 = static_cast<int>((I + kTileK - 1) / kTileK);
