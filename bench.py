@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # one decode point of each other workload and the large int8 prefill batch,
 # reported beside the headline workload
 OTHER_POINTS = (("qwen2_57b", 8), ("deepseek_v3", 16), ("mixtral8x22b_w8", 8192))
-KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_defer.cuh", "common.cuh", "ptx.cuh", "host.cu")
+KERNEL_SOURCES = ("gemm_kernel.cuh", "gemm_defer.cuh", "common.cuh", "ptx.cuh", "plan.cuh", "host.cu", "layer_plan.cu")
 
 
 def parse():
@@ -61,6 +61,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-workloads", action="store_true")
+    p.add_argument("--touched-weights", action="store_true",
+                   help="generate only the experts the headline batch routes to (profiling runs; "
+                        "implies --no-sweep, the other batches route elsewhere)")
     return p.parse_args()
 
 
@@ -294,12 +297,12 @@ def host_cores():
 
 def gemm_kernel_name(w, wl, M, gemm):
     """Name of the GEMM kernel the library launches for this workload (the
-    library's selection rule: 16-token tiles with every 128-wide K stage inside
-    one quantization group, and 4-bit codes or fp16 activations, run the
+    library's selection rule: 16- and 32-token tiles with every 128-wide K stage
+    inside one quantization group, and 4-bit codes or fp16 activations, run the
     deferred-scale kernel)."""
     block = w.choose_block(M, wl.topk, wl.E)
     g = wl.group_size
-    defer = block == 16 and (g == -1 or g >= 128) and (wl.bits == 4 or wl.act_dtype == "f16")
+    defer = block in (16, 32) and (g == -1 or g >= 128) and (wl.bits == 4 or wl.act_dtype == "f16")
     base = "moe_gemm_defer_kernel" if defer else "moe_gemm_kernel"
     return f"{base}<{wl.bits},{wl.act_dtype},{wl.scale_dtype},{gemm}>"
 
@@ -462,7 +465,11 @@ def ours_arm(args):
     M = args.M
     peaks = load_peaks()
 
-    weights = make_expert_weights(wl, dev)
+    if args.touched_weights:
+        args.no_sweep = True
+        weights = _sample_weights(wl, M, dev, tokens=M)
+    else:
+        weights = make_expert_weights(wl, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def setup(Mx, wlx=wl, weightsx=None):
