@@ -416,6 +416,8 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
       const Unit w = decode_unit(u, nb, a);
       const int n = w.kt1 - w.kt0;
+      // the epilogue's routed-pair count, fetched into L1 now (no register held)
+      if (NT == 16 && g == 0) prefetch_l1(a.block_rows + w.blk);
       float acc[NT];
 #pragma unroll
       for (int j = 0; j < NT; ++j) acc[j] = 0.f;
@@ -533,6 +535,9 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         if (defer_c_col(NT) == NT && !warp_wait_all(cempty, uc & 1, abort_flag, a.status)) break;
         continue;
       }
+      // routed pairs of the block (they lead it): 16-token epilogues skip the
+      // padding (measured: 32-token ones ran slower with the check)
+      const int rows = NT == 16 ? a.block_rows[w.blk] : NT;
       if (!warp_wait_all(cfull, uc & 1, abort_flag, a.status)) break;
       tc_fence_after();
 #pragma unroll
@@ -592,6 +597,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         }
 #pragma unroll
         for (int j = 0; j < NT / 2; ++j) {
+          if (!defer_writes_col(1, j, rows, NT)) break;  // columns j and j + NT/2: padding, as are the rest
           const float mine = lo ? acc[j] : acc[j + NT / 2];
           const float other = __shfl_xor_sync(0xFFFFFFFFu, lo ? acc[j + NT / 2] : acc[j], 16);
           const float gt = lo ? mine : other;
@@ -634,6 +640,7 @@ __global__ void __launch_bounds__(kDeferThreads, 2)
         }
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
+          if (!defer_writes_col(2, j, rows, NT)) break;  // padding from here on
           const int pid = __shfl_sync(0xFFFFFFFFu, my_pid, j);
           const float tw = __shfl_sync(0xFFFFFFFFu, my_w, j);
           if (pid >= 0 && pid < a.P && hr < a.N) {

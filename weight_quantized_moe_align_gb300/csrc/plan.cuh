@@ -186,6 +186,15 @@ WNA16_HD int defer_p_col(int g, int nt) { return g * nt; }
 WNA16_HD int defer_c_col(int nt) { return nt == 16 ? 32 : nt; }
 WNA16_HD int defer_a_col(int g) { return kDeferA0 + g * kDeferAStride; }
 
+// Token columns of a block that the deferred-scale epilogue writes (the
+// routed pairs lead a block): the gate/up epilogue finishes columns j and
+// j + nt/2 together and stops at the first j past the routed pairs; the down
+// epilogue stops at the routed pairs.
+WNA16_HD bool defer_writes_col(int gemm, int col, int rows, int nt) {
+  if (gemm == 2) return col < rows;
+  return (col < nt / 2 ? col : col - nt / 2) < rows;
+}
+
 // General kernel: accumulator i at [i*nt, +nt), A slot s at nacc*nt + s*64.
 WNA16_HD int gemm_acc_col(int acc, int nt) { return acc * nt; }
 WNA16_HD int gemm_a_col(int nacc, int nt, int slot) { return nacc * nt + slot * kASlotCols; }

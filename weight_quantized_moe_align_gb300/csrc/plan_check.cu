@@ -277,21 +277,28 @@ extern "C" int64_t wna16_check_launch_plan(int64_t M, int64_t H, int64_t I, int 
           }
         }
         // epilogue: the general kernel writes the block's routed columns
-        // rounded up to 16, the deferred-scale kernel all of them
-        const int ncols = p.defer ? B : trimmed_n(a.block_rows[w.blk], B);
-        if (ncols < block_rows[w.blk]) c.fail("GEMM %d: block %d writes %d of its %d routed columns", gemm, w.blk, ncols, block_rows[w.blk]);
+        // rounded up to 16, the deferred-scale kernel its routed columns (the
+        // gate/up one in pairs j, j + B/2)
+        const int rows = a.block_rows[w.blk];
+        auto writes = [&](int col) {
+          return p.defer ? defer_writes_col(gemm, col, rows, B) : col < trimmed_n(rows, B);
+        };
+        for (int col = 0; col < block_rows[w.blk]; ++col)
+          if (!writes(col)) c.fail("GEMM %d: block %d leaves routed column %d unwritten", gemm, w.blk, col);
         if (gemm == 1) {
           for (int q = 0; q < 4; ++q)
             for (int lane = 0; lane < 32; ++lane) {
               const int f = w.tile * kGateUpRows + 16 * q + (lane & 15);
               const int fp = bits == 4 ? permute_k8(f) : f;
               if (f >= a.I) c.fail("GEMM 1: feature %d of tile %d past I", f, w.tile);
-              for (int col = 0; col < ncols; ++col) {
+              for (int col = 0; col < B; ++col) {
+                if (!writes(col)) continue;
                 if (act_index(w.blk, B, col, a.I, fp) >= act_elems)
                   c.fail("GEMM 1: act cache element of block %d column %d feature %d past the act cache", w.blk, col, fp);
               }
               if (p.defer) {
                 for (int col = 0; col < B; ++col) {
+                  if (!writes(col)) continue;
                   const size_t row = static_cast<size_t>(w.blk) * B + col;
                   const int part = (w.tile & 1) * 8 + q * 2 + (lane & 1);
                   if (xs_out_index(w.tile, part, a.cap, row) >= xs2_elems)
@@ -307,7 +314,8 @@ extern "C" int64_t wna16_check_launch_plan(int64_t M, int64_t H, int64_t I, int 
               }
             }
         } else {
-          for (int col = 0; col < ncols; ++col) {
+          for (int col = 0; col < B; ++col) {
+            if (!writes(col)) continue;
             const int64_t si = static_cast<int64_t>(w.blk) * B + col;
             if (si >= cap) {
               c.fail("GEMM 2: sorted_ids read %lld past the capacity", (long long)si);
