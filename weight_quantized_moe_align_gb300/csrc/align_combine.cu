@@ -191,13 +191,15 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
 }
 
 // Copies the hidden row of every routed pair to its expert-sorted slot:
-// x_sorted[slot_of_pair[p]] = hidden[p / topk], one thread per 64-element
-// chunk (eight 16-byte vectors). With `permute` (int4 weights) each vector is
-// stored in the GEMM's K order 0,4,1,5,2,6,3,7. With `xs` the thread also
-// writes the fp32 sums of the chunk's even-k and odd-k values, the token sums
-// of the deferred-scale gate/up GEMM: xs[(stage * 4 + 2 * half + parity) * cap
-// + slot], stage = chunk / 2, half = chunk % 2. Padded slots are not written:
-// they only feed MMA columns whose results are discarded.
+// x_sorted[slot_of_pair[p]] = hidden[p / topk], one thread per 16-byte vector,
+// consecutive threads on consecutive vectors of a row (coalesced loads and
+// stores). With `permute` (int4 weights) each vector is stored in the GEMM's K
+// order 0,4,1,5,2,6,3,7. With `xs` the 8 lanes holding a 64-element chunk also
+// add up the fp32 sums of its even-k and odd-k values (the token sums of the
+// deferred-scale gate/up GEMM) and the chunk's first lane writes them:
+// xs[(stage * 4 + 2 * half + parity) * cap + slot], stage = chunk / 2, half =
+// chunk % 2. Padded slots are not written: they only feed MMA columns whose
+// results are discarded.
 template <int ACT>
 __device__ __forceinline__ void add_even_odd(uint32_t w, float& se, float& so) {
   if constexpr (ACT == 0) {
@@ -218,42 +220,50 @@ __global__ void __launch_bounds__(256)
                       float* __restrict__ zero3, int zero_n3) {
   grid_dep_wait();
   grid_dep_launch();
-  const int chunks = h8 / 8;
-  const long long n = static_cast<long long>(P) * chunks;
+  // h8 (16-byte vectors per row) is a multiple of 8 and the stride a multiple
+  // of 256: the 8 lanes of a chunk always share one pair and one iteration
+  const long long n = static_cast<long long>(P) * h8;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long first = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (long long idx = first; idx < n; idx += stride) {
-    const int p = static_cast<int>(idx / chunks);
-    const int c = static_cast<int>(idx % chunks);
+  const unsigned chunk_lanes = 0xFFu << (threadIdx.x & 24);
+  // (pair, vector) of idx, advanced by the stride without a division per step
+  const int sp = static_cast<int>(stride / h8), sv = static_cast<int>(stride % h8);
+  int p = static_cast<int>(first / h8), v = static_cast<int>(first % h8);
+  for (long long idx = first; idx < n; idx += stride, p += sp, v += sv) {
+    if (v >= h8) {
+      v -= h8;
+      ++p;
+    }
     const int e = ids[p];
     if (e < 0 || e >= E) continue;
     const int slot = slot_of_pair[p];
-    const uint4* src = hidden + static_cast<long long>(p / topk) * h8 + c * 8;
-    uint4* dst = x_sorted + static_cast<long long>(slot) * h8 + c * 8;
-    float se = 0.f, so = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint4 v = src[i];
-      if (xs) {
-        add_even_odd<ACT>(v.x, se, so);
-        add_even_odd<ACT>(v.y, se, so);
-        add_even_odd<ACT>(v.z, se, so);
-        add_even_odd<ACT>(v.w, se, so);
-      }
-      if (permute) {  // (x0 x1)(x2 x3)(x4 x5)(x6 x7) -> (x0 x4)(x1 x5)(x2 x6)(x3 x7)
-        const uint4 u = v;
-        v.x = __byte_perm(u.x, u.z, 0x5410);
-        v.y = __byte_perm(u.x, u.z, 0x7632);
-        v.z = __byte_perm(u.y, u.w, 0x5410);
-        v.w = __byte_perm(u.y, u.w, 0x7632);
-      }
-      dst[i] = v;
-    }
+    uint4 x = hidden[static_cast<long long>(p / topk) * h8 + v];
     if (xs) {
-      const long long base = (static_cast<long long>(c >> 1) * 4 + (c & 1) * 2) * cap + slot;
-      xs[base] = se;
-      xs[base + cap] = so;
+      float se = 0.f, so = 0.f;
+      add_even_odd<ACT>(x.x, se, so);
+      add_even_odd<ACT>(x.y, se, so);
+      add_even_odd<ACT>(x.z, se, so);
+      add_even_odd<ACT>(x.w, se, so);
+#pragma unroll
+      for (int m = 1; m < 8; m <<= 1) {
+        se += __shfl_xor_sync(chunk_lanes, se, m);
+        so += __shfl_xor_sync(chunk_lanes, so, m);
+      }
+      if ((v & 7) == 0) {
+        const int c = v >> 3;
+        const long long base = (static_cast<long long>(c >> 1) * 4 + (c & 1) * 2) * cap + slot;
+        xs[base] = se;
+        xs[base + cap] = so;
+      }
     }
+    if (permute) {  // (x0 x1)(x2 x3)(x4 x5)(x6 x7) -> (x0 x4)(x1 x5)(x2 x6)(x3 x7)
+      const uint4 u = x;
+      x.x = __byte_perm(u.x, u.z, 0x5410);
+      x.y = __byte_perm(u.x, u.z, 0x7632);
+      x.z = __byte_perm(u.y, u.w, 0x5410);
+      x.w = __byte_perm(u.y, u.w, 0x7632);
+    }
+    x_sorted[static_cast<long long>(slot) * h8 + v] = x;
   }
   for (long long i = first; i < zero_n0; i += stride) zero0[i] = 0.f;
   for (long long i = first; i < zero_n1; i += stride) zero1[i] = 0.f;
@@ -306,34 +316,36 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
-// One thread per 4 consecutive outputs of one token.
+// One thread per 4 consecutive output columns, for the tokens blockIdx.y,
+// blockIdx.y + gridDim.y, ...: out[t] = sum over the slots (and K splits) of
+// the fp32 rows, in slot order, rounded once.
 template <typename T>
 __global__ void __launch_bounds__(256)
     moe_combine_kernel(const float* __restrict__ slab, const int32_t* __restrict__ ids, int M, int H,
                        int topk, int E, int split, int summed, T* __restrict__ out) {
   grid_dep_wait();
-  const int h4 = H / 4;
-  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<long long>(M) * h4) return;
-  const int t = static_cast<int>(idx / h4);
-  const int h = static_cast<int>(idx % h4) * 4;
+  // x: 4-column vectors of a row, y: tokens (strided when M exceeds the grid)
+  const int h = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (h >= H) return;
   const long long P = static_cast<long long>(M) * topk;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  // summed: the down GEMM already added the slots and splits into [M, H]
-  if (summed) acc = *reinterpret_cast<const float4*>(slab + static_cast<long long>(t) * H + h);
-  for (int j = 0; j < (summed ? 0 : topk); ++j) {
-    const int e = ids[t * topk + j];
-    if (e < 0 || e >= E) continue;  // dropped pair
-    for (int s = 0; s < split; ++s) {
-      const float4 v = *reinterpret_cast<const float4*>(slab + ((s * P) + t * topk + j) * H + h);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+  for (int t = blockIdx.y; t < M; t += gridDim.y) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // summed: the down GEMM already added the slots and splits into [M, H]
+    if (summed) acc = *reinterpret_cast<const float4*>(slab + static_cast<long long>(t) * H + h);
+    for (int j = 0; j < (summed ? 0 : topk); ++j) {
+      const int e = ids[t * topk + j];
+      if (e < 0 || e >= E) continue;  // dropped pair
+      for (int s = 0; s < split; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(slab + ((s * P) + static_cast<long long>(t) * topk + j) * H + h);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
     }
+    T o[4] = {from_f32<T>(acc.x), from_f32<T>(acc.y), from_f32<T>(acc.z), from_f32<T>(acc.w)};
+    *reinterpret_cast<uint2*>(out + static_cast<long long>(t) * H + h) = *reinterpret_cast<uint2*>(o);
   }
-  T o[4] = {from_f32<T>(acc.x), from_f32<T>(acc.y), from_f32<T>(acc.z), from_f32<T>(acc.w)};
-  *reinterpret_cast<uint2*>(out + static_cast<long long>(t) * H + h) = *reinterpret_cast<uint2*>(o);
 }
 
 cudaError_t launch_align(const int32_t* ids, int P, int E, int block, int cap, int32_t* sorted_ids,
@@ -378,8 +390,9 @@ cudaError_t launch_gather(const void* hidden, const int32_t* ids, const int32_t*
                           float* xs, int cap, float* zero_ptr0, int zero_n0, float* zero_ptr1, int zero_n1,
                           float* zero_ptr2, int zero_n2, float* zero_ptr3, int zero_n3, cudaStream_t stream,
                           bool pdl) {
-  const int h8 = H / 8;
-  long long n = static_cast<long long>(P) * (h8 / 8);
+  const int h8 = H / 8;  // a multiple of 8 (H % 64 == 0): the kernel's chunk lanes rely on it
+  if (h8 % 8) return cudaErrorInvalidValue;
+  long long n = static_cast<long long>(P) * h8;
   n = std::max<long long>(n, std::max({zero_n0, zero_n1, zero_n2, zero_n3}));
   const int threads = 256;
   const long long want = (n + threads - 1) / threads;
@@ -406,13 +419,13 @@ cudaError_t launch_gather_perm(const void* hidden, const int32_t* ids, const int
 
 cudaError_t launch_combine(const float* slab, const int32_t* ids, int M, int H, int topk, int E,
                            int split, int summed, int act_dtype, void* out, cudaStream_t stream, bool pdl) {
-  const long long n = static_cast<long long>(M) * (H / 4);
   const int threads = 256;
-  const unsigned blocks = static_cast<unsigned>((n + threads - 1) / threads);
+  const dim3 blocks((H / 4 + threads - 1) / threads, static_cast<unsigned>(std::min(M, 65535)));
+  if (M <= 0) return cudaSuccess;
   if (act_dtype == 0)
-    return launch_kernel(moe_combine_kernel<__half>, dim3(blocks), dim3(threads), 0, stream, pdl, slab, ids, M, H,
+    return launch_kernel(moe_combine_kernel<__half>, blocks, dim3(threads), 0, stream, pdl, slab, ids, M, H,
                          topk, E, split, summed, static_cast<__half*>(out));
-  return launch_kernel(moe_combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, stream, pdl, slab, ids, M,
+  return launch_kernel(moe_combine_kernel<__nv_bfloat16>, blocks, dim3(threads), 0, stream, pdl, slab, ids, M,
                        H, topk, E, split, summed, static_cast<__nv_bfloat16*>(out));
 }
 
