@@ -11,16 +11,22 @@
 // for a single decode token.
 //
 // Pipeline per CTA (persistent over units; every wait is time-bounded):
-//   TMA warp:      packed weights/scales/zeros of stage s  -> smem ring  (wfull[s])
-//   gather warps:  token rows (cp.async, zero fill for pad) -> smem ring (bfull[s])
-//   dequant warps: smem codes -> fp16/bf16 -> tcgen05.st into a TMEM A slot (afull)
-//   MMA warp:      4 x tcgen05.mma K=16 per stage, commits empty[s], aempty[slot]
-//   epilogue:      TMEM accumulator -> silu(gate)*up -> act cache   (gate/up GEMM)
-//                  TMEM accumulator * topk weight -> fp32 slab row  (down GEMM)
-// Each K stage spans 64 elements and lies inside one quantization group
-// (group size a multiple of 64): the per-stage scale is the scale of the group
-// that K range belongs to (the BLOCK_SIZE_K vs group-size hazard reported on
-// vLLM PR #6502 cannot occur).
+//   TMA producer:  per 128-wide K stage, the packed codes of 128 weight rows,
+//                  their scales and zero points, and the stage's token tile
+//                  (two 64-wide K chunks of the block's rows) -> ring slot s
+//                  (full[s])
+//   dequant warps: two warpgroups taking alternate stages: smem codes ->
+//                  round((u - z) * s) in fp16/bf16 -> tcgen05.st into a TMEM
+//                  A slot (afull)
+//   MMA warp:      8 x tcgen05.mma K=16 per stage, N = the block's routed
+//                  pairs rounded up to 16; commits empty[s] (frees the ring
+//                  slot and the stage's A slot) and, per unit, accfull
+//   epilogue:      four warps: TMEM accumulator -> silu(gate)*up -> act cache
+//                  (gate/up GEMM), or * top-k weight -> fp32 slab row (down)
+// A K stage spans 128 elements inside one quantization group, or two groups
+// of 64 (group size 64 or a multiple of 128): the per-stage scale rows are
+// those of the groups the stage covers (the BLOCK_SIZE_K vs group-size hazard
+// reported on vLLM PR #6502 cannot occur).
 #pragma once
 
 #include <cuda_bf16.h>
